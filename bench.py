@@ -1,0 +1,409 @@
+"""Benchmark of the paged-KV decode step (decode_paged) on GB300.
+
+One step = one pkv_decode call over a batch: QK-norm + RoPE + KV append for
+every row, split-KV attention over each row's pages, and the split combine.
+The default workload is 64 rows with context lengths U[512, 4096] at
+Qwen3-8B attention shapes (32 query heads, 8 kv heads, head_dim 128, pages of
+64), synthetic and seeded.  Metric: decode rows/s (and the KV-read GB/s it
+implies), with the attention kernel's achieved HBM bandwidth against the
+measured copy bandwidth of the chip.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload config2|config3|config4|sweepRxL]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch of the
+same shape (weak scaling, no data-path collective); the timed region is
+bracketed by barriers and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode_paged rows/s and KV-read GB/s vs GB300 HBM roofline (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment (1 process if absent)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch of the same shape (weak scaling)."""
+    return base_seed + 7919 * rank
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- workloads
+
+def make_workload(name: str, rank: int = 0):
+    import workloads as W
+    if name == "config2":
+        wl = W.make_decode("decode 64 rows x U[512,4096]", (64, 512, 4096), seed=rank_seed(1002, rank),
+                           table_pages=64)
+    elif name == "config3":
+        wl = W.make_decode("long-context decode 8 rows x U[32768,40960]", (8, 32768, 40960),
+                           seed=rank_seed(1003, rank), table_pages=640)
+    elif name == "config4":
+        wl = W.make_decode("shared-prefix decode 256 rows x U[1024,8192], groups of 16 share 8-32 pages",
+                           (256, 1024, 8192), seed=rank_seed(1004, rank), table_pages=128, share_groups=16)
+    elif name.startswith("sweep"):
+        r, l = name[5:].split("x")
+        wl = W.sweep(int(r), int(l), seed=rank_seed(2000 + int(r) + int(l), rank))
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    return wl
+
+
+# ---------------------------------------------------------------------------- measurement helpers
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in d:
+                v = d[key]
+                v = v.get("value", v) if isinstance(v, dict) else v
+                return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "paged_kv_gqa_qk_gb300", "csrc", "pkv_kernels.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if the kernel is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "attn_decode_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sha") != kernel_source_hash() or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def attention_algorithmic_bytes(wl) -> int:
+    """Bytes the attention kernel must move per launch: K and V of every attended
+    position (4096 B each at 8 kv heads x 128 x bf16 x 2), each row's page-table
+    entries, its normed q (fp32) and its bf16 output."""
+    import workloads as W
+    S = wl.cfg["page_size"]
+    L = [int(p) + 1 for p in wl.step_positions.tolist() if p >= 0]
+    kv = W.kv_bytes_per_position(wl.cfg) * sum(L)
+    table = 4 * sum(-(-x // S) for x in L)
+    H, D = wl.cfg["heads"], wl.cfg["head_dim"]
+    return kv + table + len(L) * H * D * (4 + 2)
+
+
+# ---------------------------------------------------------------------------- the GPU arm
+
+def run_gpu(args) -> None:
+    import torch
+    import paged_kv_gqa_qk_gb300 as pkv
+
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    pkv.load_library()
+
+    wl = make_workload(args.workload, rank)
+    R, pages = wl.R, wl.pages
+    K, V = wl.K0.to(dev), wl.V0.to(dev)
+    pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+    q, k, v, qw, kw, pos, tab = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w,
+                                                    wl.step_positions, wl.table))
+    out = torch.empty_like(q)
+    ws = pool.workspace(R, pages, 0)
+    stream = torch.cuda.Stream(device=dev)
+    nsplit_gt1 = True  # combine launches whenever the plan has more than one split column
+
+    def step():
+        pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, out, ws, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    flags = pkv.pkv_check_errors(pool.handle, stream)
+    if flags:
+        raise SystemExit(f"device error flags {flags}")
+
+    # ---- device-timed region: inputs resident in HBM
+    pkv.pkv_timer_enable(pool.handle, True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = ev0.elapsed_time(ev1)
+    attn_ms, attn_n = pkv.pkv_timer_read(pool.handle)
+    pkv.pkv_timer_enable(pool.handle, False)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+
+    # ---- end-to-end through the C ABI with host buffers: inputs H2D from pinned
+    # memory and the output D2H, every step, inside the timed region
+    host_in = [t.pin_memory() for t in (wl.q, wl.k, wl.v, wl.step_positions, wl.table)]
+    dev_in = [q, k, v, pos, tab]
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+    flags = pkv.pkv_check_errors(pool.handle, stream)
+    if flags:
+        raise SystemExit(f"device error flags {flags}")
+
+    plan_bytes = attention_algorithmic_bytes(wl)
+    attn_avg_s = attn_ms / 1e3 / max(attn_n, 1)
+    achieved = plan_bytes / attn_avg_s / 1e9
+    peak, peak_kind = measured_peak_hbm()
+    logical = wl.meta["logical_kv_bytes"]
+    launches_per_step = 3
+    rows_total = R * world
+    res = {
+        "metric": METRIC,
+        "value": rows_total / (ms_step / 1e3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v/cache, U[0.5,1.5] norm weights, shuffled pages)",
+        "config": {"workload": wl.name, "rows": R, "table_pages": pages, "pool_pages": wl.num_pages,
+                   "heads": wl.cfg["heads"], "kv_heads": wl.cfg["kv_heads"], "head_dim": wl.cfg["head_dim"],
+                   "page_size": wl.cfg["page_size"], "sum_context": sum(wl.meta["lengths"]),
+                   "kv_bytes_per_step": logical,
+                   "l2": f"inputs larger than L2: {logical / 1e9:.2f} GB of K/V per step vs 126 MB L2",
+                   "parallelism": f"dp{world} (independent replicas, rows sharded by rank)"},
+        "kv_gbs": logical / (ms_step / 1e3) / 1e9 * world,
+        "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(args.workload), "algorithmic_bytes_per_launch": plan_bytes,
+                     "avg_launch_us": attn_avg_s * 1e6, "timed_launches": attn_n},
+        "e2e": {"value": rows_total * args.steps / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    pool.close()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- the oracle (CPU)
+
+def _oracle_step(wl, rows, K, V, args_bits, nthreads):
+    import numpy as np
+    import oracle
+    sel = np.asarray(rows, dtype=np.int32)
+    oracle.decode(K, V, *args_bits, wl.step_positions.numpy(), wl.table.numpy(), cfg=wl.cfg, sel=sel,
+                  nthreads=nthreads)
+
+
+def cpu_baseline(wl, budget_s: float = 10.0) -> dict:
+    """The fp64 oracle, as it stands, on the host's cores: whole decode steps over
+    a bounded sample of the rows (the first rows of the same batch), repeated
+    until about budget_s seconds of CPU work."""
+    import workloads as W
+    nthreads = os.cpu_count() or 1
+    K, V = W.bits(wl.K0).copy(), W.bits(wl.V0).copy()
+    args_bits = [W.bits(t) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w)]
+    n = min(wl.R, 8)
+    rows = list(range(n))
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        _oracle_step(wl, rows, K, V, args_bits, nthreads)
+        done += n
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 64 * wl.R:
+            break
+    return {"value": done / el, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{n} rows (all 32 heads) of the same batch per pass, {done // n} passes, {el:.1f} s; "
+                      f"every pass also writes all {wl.R} rows' k/v"}
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    wl = make_workload(args.workload, 0)
+    nthreads = os.cpu_count() or 1
+    K, V = W.bits(wl.K0).copy(), W.bits(wl.V0).copy()
+    args_bits = [W.bits(t) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w)]
+    n = min(wl.R, 8)
+    rows = list(range(n))
+    for _ in range(args.warmup):
+        _oracle_step(wl, rows, K, V, args_bits, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(wl, rows, K, V, args_bits, nthreads)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    res = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded workload as the GPU arm)",
+        "config": {"workload": wl.name, "rows": wl.R, "table_pages": wl.pages,
+                   "sample_rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{n} rows (all 32 heads) of the batch per step; each step also writes all "
+                                   f"{wl.R} rows' k/v"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--workload", default="config2")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

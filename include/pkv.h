@@ -1,0 +1,227 @@
+/*
+ * pkv.h -- C ABI of libpkv: the paged-KV decode step of a Qwen3-style
+ * attention layer on one GB300 (sm_103a).
+ *
+ * What the library computes is the attention half of the Qwen3-8B Nest
+ * package's paged entries (qwen3-8b Nest files, src/attention.linnet,
+ * GroupedQueryAttention.decode_paged and .step_paged; README.md, Entries):
+ * for every token it
+ *   1. applies per-head QK-norm, RMS normalisation of each head's head_dim
+ *      slice with eps 1e-6 and a [head_dim] weight, to q and k (not v)
+ *      (README.md; src/norm.linnet RmsNorm);
+ *   2. rotates the normed q and k with rotate-half RoPE, base 1e6
+ *      (src/rope.linnet tables; decode_paged's rope_rows);
+ *   3. writes k and v at the token's slot of the page pool,
+ *      slot = table[row][pos / page_size] * page_size + pos % page_size
+ *      (decode_paged's page_slots + write_tokens);
+ *   4. attends: query head h reads kv head h / (heads / kv_heads) over the
+ *      row's positions 0..pos inclusive, scale 1/sqrt(head_dim)
+ *      (decode_paged's paged_attention; decode_rows' mask s <= positions[b]).
+ * The q/k/v projections before and the output projection after are not part
+ * of this library: callers pass the projected q, k, v split into heads
+ * (split_heads: [tokens][heads][head_dim]) and receive the attention output in
+ * the same layout (merge_heads of it is a reshape).
+ *
+ * Conventions shared by every entry point.
+ *   - bf16 tensors are passed as void pointers to IEEE bfloat16 data.
+ *   - "device" pointers must point into memory of the current CUDA device;
+ *     "host" pointers into ordinary host memory.  The caller owns every
+ *     tensor it passes; the library never frees them.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  pkv_decode
+ *     and pkv_step only enqueue work on it: they neither allocate nor
+ *     synchronise, and return before the GPU has run.
+ *   - Errors a host check can see (null pointers, sizes, a workspace that is
+ *     too small, an unsupported configuration) are returned synchronously as
+ *     negative PKV_E* codes and nothing is enqueued.  Errors that depend on
+ *     device-resident data (positions, page ids, slots) are caught on the
+ *     device: the token is skipped (no write, zero output) and a bit is set
+ *     in the pool's sticky error word, read with pkv_check_errors().  No
+ *     kernel traps or spins without bound.
+ *   - The kernels are built for head_dim 128, page_size 64 and
+ *     heads == 4 * kv_heads (Qwen3-8B: 32 query heads over 8 kv heads); other
+ *     shapes are rejected with PKV_ENOTIMPL at pool creation.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---------------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_EINVAL (-1)     /* null pointer, non-positive size, misaligned buffer, bad config */
+#define PKV_ERANGE (-2)     /* a size beyond what the library supports */
+#define PKV_ENOMEM (-3)     /* device allocation failed (pool creation only) */
+#define PKV_ECUDA (-4)      /* a CUDA runtime call failed */
+#define PKV_EWORKSPACE (-5) /* workspace smaller than pkv_workspace_bytes() */
+#define PKV_EDEVICE (-6)    /* no usable device, or the pool lives on another device */
+#define PKV_ENOTIMPL (-7)   /* configuration the kernels are not built for */
+
+/* ---- bits of the sticky device error word (pkv_check_errors) ---------------- */
+#define PKV_DEVERR_POSITION 1u /* position < 0 (other than a -1 "no step"), >= max_seq, or >= pages*page_size */
+#define PKV_DEVERR_PAGE 2u     /* a table entry the token reads is not in [0, num_pages) */
+#define PKV_DEVERR_ROW 4u      /* a prompt token's row is not in [0, rows) */
+#define PKV_DEVERR_SLOT 8u     /* an explicit prompt slot is not in [0, num_pages*page_size) */
+#define PKV_DEVERR_TIMEOUT 16u /* a bounded device wait gave up (results of that call are void) */
+
+/* ---- configuration ----------------------------------------------------------
+ * Shape of one attention layer.  Defaults (pkv_config_default) are Qwen3-8B's:
+ * qwen3-8b Nest files, nest.toml [generics] (Heads 32, KvHeads 8, HeadDim 128,
+ * MaxSeq 40960), src/attention.linnet (PageSize 64), src/rope.linnet (THETA
+ * 1e6), src/norm.linnet (eps 1e-6). */
+typedef struct {
+    int heads;         /* query heads per token */
+    int kv_heads;      /* key/value heads per token */
+    int head_dim;      /* elements per head vector */
+    int page_size;     /* positions per page */
+    int max_seq;       /* positions must be < max_seq (length of the RoPE table) */
+    double rope_theta; /* RoPE base */
+    double eps;        /* QK-norm epsilon */
+} pkv_config;
+
+/* Fill *cfg with the Qwen3-8B defaults.  Returns PKV_OK or PKV_EINVAL (null). */
+PKV_API int pkv_config_default(pkv_config* cfg);
+
+/* Human-readable name of a return code (static string, never NULL). */
+PKV_API const char* pkv_strerror(int code);
+
+/* ---- the page pool ------------------------------------------------------------
+ * The pool is the layer's KV cache: with Batch 1 the cache's one row is a pool
+ * of pages, page_size positions each, that rows reference through a page
+ * table (README.md, Entries, decode_paged; src/lib.linnet Model.decode_paged).
+ *
+ * Layout of K and V (each): bf16 [kv_heads][num_pages * page_size][head_dim],
+ * row-major.  Position s of page p for kv head g is element
+ * ((g * num_pages + p) * page_size + s) * head_dim.  For one kv head a page is
+ * one contiguous block of page_size * head_dim * 2 bytes (16 KiB).
+ *
+ * A pool also holds the RoPE (cos, sin) table for positions 0..max_seq-1
+ * (double precision, computed on the host; 16 bytes x head_dim/2 x max_seq,
+ * 42 MB at the defaults) and the sticky device error word. */
+typedef struct pkv_pool pkv_pool;
+
+/* Create a pool that owns num_pages pages of K and V on the current device
+ * (contents zeroed).  stream orders the initialisation.  *out receives the
+ * pool; free it with pkv_pool_free.
+ * Errors: PKV_EINVAL (null cfg/out, num_pages <= 0, bad config values),
+ * PKV_ENOTIMPL (shape other than head_dim 128 / page_size 64 /
+ * heads == 4*kv_heads), PKV_ERANGE (num_pages*page_size >= 2^31 or max_seq >
+ * 2^20), PKV_ENOMEM, PKV_EDEVICE, PKV_ECUDA. */
+PKV_API int pkv_pool_alloc(const pkv_config* cfg, int num_pages, void* stream, pkv_pool** out);
+
+/* Create a pool over caller-owned K and V buffers (device pointers, layout as
+ * above, 256-byte aligned).  The pool borrows them: the caller keeps them
+ * alive until pkv_pool_free and frees them itself.  Their contents are left
+ * as they are.  Errors as pkv_pool_alloc, plus PKV_EINVAL for a null or
+ * misaligned k/v. */
+PKV_API int pkv_pool_wrap(const pkv_config* cfg, int num_pages, void* k, void* v, void* stream, pkv_pool** out);
+
+/* Release the pool (and its K/V if it owns them).  Waits for the device to
+ * finish using it.  NULL is accepted and ignored. */
+PKV_API int pkv_pool_free(pkv_pool* pool);
+
+/* The pool's K and V device pointers and its number of slots
+ * (num_pages * page_size).  Any output pointer may be NULL. */
+PKV_API int pkv_pool_kv(const pkv_pool* pool, void** k, void** v, int64_t* num_slots);
+
+/* ---- workspace ------------------------------------------------------------------
+ * Scratch device memory a call needs, in bytes, for `tokens = prefill_tokens +
+ * rows` tokens and a page table `pages` wide.  The caller allocates it (256-byte
+ * aligned) and passes it to pkv_decode / pkv_step; its contents need no
+ * initialisation and are not meaningful after the call.  The size depends
+ * only on (pool config, rows, pages, prefill_tokens).
+ * Errors: PKV_EINVAL (null, rows < 0, prefill_tokens < 0, both zero,
+ * pages <= 0), PKV_ERANGE (too many tokens). */
+PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_tokens, size_t* bytes);
+
+/* ---- decode_paged ------------------------------------------------------------------
+ * qwen3-8b Nest files, src/attention.linnet GroupedQueryAttention.decode_paged
+ * (steps 1-4 above) for `rows` rows, one new token each.  Row b's token sits
+ * at position positions[b]; its key and value are written to
+ *   slot = table[b][positions[b] / page_size] * page_size + positions[b] % page_size
+ * and its query attends over positions 0..positions[b] of the row, read
+ * through table[b] (so it sees its own new key).  All writes of the call
+ * happen before any attention.
+ *
+ *   q         device bf16 [rows][heads][head_dim]     (projected, split into heads)
+ *   k, v      device bf16 [rows][kv_heads][head_dim]
+ *   q_norm_w  device bf16 [head_dim]                  (QK-norm weights)
+ *   k_norm_w  device bf16 [head_dim]
+ *   positions device int32 [rows]; -1 = the row takes no step (no write,
+ *             zero output, not an error) -- the pages' own convention, a row
+ *             that lists a scratch page, works as well
+ *   table     device int32 [rows][pages], row-major; entries past a row's
+ *             last page are never read
+ *   out       device bf16 [rows][heads][head_dim]
+ *   workspace device, >= pkv_workspace_bytes(pool, rows, pages, 0), 256-byte aligned
+ *
+ * Slots written by one call must be distinct (the pages' write_tokens is a
+ * scatter); if two tokens write one slot, which value lands is unspecified.
+ * Returns PKV_OK once the work is enqueued, or a PKV_E* code with nothing
+ * enqueued. */
+PKV_API int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+               const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows, int pages,
+               void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- step_paged ----------------------------------------------------------------------
+ * qwen3-8b Nest files, src/attention.linnet GroupedQueryAttention.step_paged:
+ * P prompt tokens packed end to end (prefill_paged) and one step for each of
+ * `rows` rows (decode_paged) in one pass.  Token order is the P prompt tokens,
+ * then the rows' step tokens.  Prompt token p sits at position positions[p]
+ * of table row prow[p] and is written at slots[p]; row b's step token sits at
+ * step_positions[b].  All P + rows tokens are normed, roped and written
+ * first; then prompt token p attends over table[prow[p]] for positions
+ * 0..positions[p] (its own chunk's earlier keys included), and row b over
+ * 0..step_positions[b].
+ *
+ *   q              device bf16 [P + rows][heads][head_dim]
+ *   k, v           device bf16 [P + rows][kv_heads][head_dim]
+ *   positions      device int32 [P]
+ *   prow           device int32 [P]    (the pages' `rows` argument)
+ *   slots          device int32 [P], or NULL: derive each slot from the table
+ *   step_positions device int32 [rows]; -1 = row takes no step
+ *   table          device int32 [rows][pages]
+ *   out            device bf16 [P + rows][heads][head_dim] (prompts, then steps)
+ *   workspace      >= pkv_workspace_bytes(pool, rows, pages, P)
+ * The pages require P > 0 and rows > 0 (PKV_EINVAL otherwise).  Slot
+ * uniqueness as for pkv_decode. */
+PKV_API int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+             const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
+             const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- errors ------------------------------------------------------------------------------
+ * Synchronise `stream`, then read and clear the pool's sticky device error
+ * word (PKV_DEVERR_* bits of every call since the last read) into *flags.
+ * Returns PKV_ECUDA if the stream reports a CUDA error. */
+PKV_API int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags);
+
+/* ---- tuning and measurement ---------------------------------------------------------------
+ * Pages each split of the split-KV attention covers (0 = automatic, chosen
+ * from the SM count, rows and table width).  Results do not depend on it
+ * beyond floating-point association.  Errors: PKV_EINVAL (null, < 0). */
+PKV_API int pkv_set_split_pages(pkv_pool* pool, int pages_per_split);
+
+/* Kernel timer: while enabled, every pkv_decode / pkv_step records a pair of
+ * CUDA events on its stream around the split-KV attention kernel (the
+ * dominant launch).  pkv_timer_read synchronises on the last recorded event,
+ * returns the summed duration in milliseconds and the number of timed
+ * launches since the timer was last enabled, and keeps the timer running.
+ * At most 4096 launches are kept (later ones overwrite the oldest). */
+PKV_API int pkv_timer_enable(pkv_pool* pool, int enable);
+PKV_API int pkv_timer_read(pkv_pool* pool, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

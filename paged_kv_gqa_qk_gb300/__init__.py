@@ -1,0 +1,260 @@
+"""Python binding of libpkv, the paged-KV decode step for GB300 (sm_103a).
+
+The functions here have the names of the C ABI in ``include/pkv.h`` and do
+argument marshalling only: they check dtypes, devices and contiguity of torch
+tensors and pass their data pointers (and the current CUDA stream) to the
+library.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback.  If ``libpkv.so`` has not been built, importing the
+binding's functions raises.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK, PKV_EINVAL, PKV_ERANGE, PKV_ENOMEM, PKV_ECUDA, PKV_EWORKSPACE, PKV_EDEVICE, PKV_ENOTIMPL = \
+    0, -1, -2, -3, -4, -5, -6, -7
+PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+
+# Every symbol include/pkv.h declares.
+ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
+               "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_check_errors",
+               "pkv_set_split_pages", "pkv_timer_enable", "pkv_timer_read")
+
+
+class PkvConfig(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int), ("kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("page_size", ctypes.c_int), ("max_seq", ctypes.c_int),
+                ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {pkv_strerror(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpkv.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpkv.so not found at {path}: build it first (python -c 'import __graft_entry__ as g; "
+                           f"g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    cfgp = ctypes.POINTER(PkvConfig)
+    sig = {
+        "pkv_config_default": ([cfgp], i32),
+        "pkv_strerror": ([i32], ctypes.c_char_p),
+        "pkv_pool_alloc": ([cfgp, i32, vp, ctypes.POINTER(vp)], i32),
+        "pkv_pool_wrap": ([cfgp, i32, vp, vp, vp, ctypes.POINTER(vp)], i32),
+        "pkv_pool_free": ([vp], i32),
+        "pkv_pool_kv": ([vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64)], i32),
+        "pkv_workspace_bytes": ([vp, i32, i32, i32, ctypes.POINTER(sz)], i32),
+        "pkv_decode": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp], i32),
+        "pkv_step": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp], i32),
+        "pkv_check_errors": ([vp, vp, ctypes.POINTER(ctypes.c_uint32)], i32),
+        "pkv_set_split_pages": ([vp, i32], i32),
+        "pkv_timer_enable": ([vp, i32], i32),
+        "pkv_timer_read": ([vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != PKV_OK:
+        raise PkvError(rc, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor | None, dtype: torch.dtype, what: str, allow_none: bool = False) -> ctypes.c_void_p:
+    if t is None:
+        if allow_none:
+            return ctypes.c_void_p(None)
+        raise ValueError(f"{what} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ------------------------------------------------------------------ C ABI, one function each
+
+def pkv_strerror(code: int) -> str:
+    return load_library().pkv_strerror(int(code)).decode()
+
+
+def pkv_config_default() -> PkvConfig:
+    c = PkvConfig()
+    _check(load_library().pkv_config_default(ctypes.byref(c)), "pkv_config_default")
+    return c
+
+
+def _cfg(cfg) -> PkvConfig:
+    if cfg is None:
+        return pkv_config_default()
+    if isinstance(cfg, PkvConfig):
+        return cfg
+    c = pkv_config_default()
+    for k, v in dict(cfg).items():
+        setattr(c, k, v)
+    return c
+
+
+def pkv_pool_alloc(cfg, num_pages: int, stream=None) -> ctypes.c_void_p:
+    out = ctypes.c_void_p()
+    _check(load_library().pkv_pool_alloc(ctypes.byref(_cfg(cfg)), int(num_pages), _stream(stream),
+                                         ctypes.byref(out)), "pkv_pool_alloc")
+    return out
+
+
+def pkv_pool_wrap(cfg, num_pages: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> ctypes.c_void_p:
+    out = ctypes.c_void_p()
+    _check(load_library().pkv_pool_wrap(ctypes.byref(_cfg(cfg)), int(num_pages), _dev(k, torch.bfloat16, "k"),
+                                        _dev(v, torch.bfloat16, "v"), _stream(stream), ctypes.byref(out)),
+           "pkv_pool_wrap")
+    return out
+
+
+def pkv_pool_free(pool) -> None:
+    _check(load_library().pkv_pool_free(pool), "pkv_pool_free")
+
+
+def pkv_pool_kv(pool):
+    k, v, n = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int64()
+    _check(load_library().pkv_pool_kv(pool, ctypes.byref(k), ctypes.byref(v), ctypes.byref(n)), "pkv_pool_kv")
+    return k.value, v.value, n.value
+
+
+def pkv_workspace_bytes(pool, rows: int, pages: int, prefill_tokens: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().pkv_workspace_bytes(pool, int(rows), int(pages), int(prefill_tokens), ctypes.byref(n)),
+           "pkv_workspace_bytes")
+    return n.value
+
+
+def pkv_decode(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, workspace, stream=None) -> None:
+    rows, pages = int(table.shape[0]), int(table.shape[1])
+    _check(load_library().pkv_decode(
+        pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
+        _dev(positions, torch.int32, "positions"), _dev(table, torch.int32, "table"), rows, pages,
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)), "pkv_decode")
+
+
+def pkv_step(pool, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out, workspace,
+             stream=None) -> None:
+    P = int(positions.shape[0])
+    rows, pages = int(table.shape[0]), int(table.shape[1])
+    _check(load_library().pkv_step(
+        pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
+        _dev(positions, torch.int32, "positions"), _dev(prow, torch.int32, "prow"),
+        _dev(slots, torch.int32, "slots", allow_none=True), _dev(step_positions, torch.int32, "step_positions"),
+        _dev(table, torch.int32, "table"), P, rows, pages, _dev(out, torch.bfloat16, "out"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "pkv_step")
+
+
+def pkv_check_errors(pool, stream=None) -> int:
+    f = ctypes.c_uint32()
+    _check(load_library().pkv_check_errors(pool, _stream(stream), ctypes.byref(f)), "pkv_check_errors")
+    return f.value
+
+
+def pkv_set_split_pages(pool, pages_per_split: int) -> None:
+    _check(load_library().pkv_set_split_pages(pool, int(pages_per_split)), "pkv_set_split_pages")
+
+
+def pkv_timer_enable(pool, enable: bool) -> None:
+    _check(load_library().pkv_timer_enable(pool, 1 if enable else 0), "pkv_timer_enable")
+
+
+def pkv_timer_read(pool):
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    _check(load_library().pkv_timer_read(pool, ctypes.byref(ms), ctypes.byref(n)), "pkv_timer_read")
+    return ms.value, n.value
+
+
+# ------------------------------------------------------------------ convenience (marshalling only)
+
+class PagedKVPool:
+    """A pool over caller-owned K/V torch tensors [kv_heads][num_pages*page_size][head_dim] (bf16)."""
+
+    def __init__(self, K: torch.Tensor, V: torch.Tensor, cfg=None, stream=None):
+        c = _cfg(cfg)
+        if K.shape != V.shape or K.dim() != 3 or K.shape[0] != c.kv_heads or K.shape[2] != c.head_dim \
+                or K.shape[1] % c.page_size:
+            raise ValueError(f"K/V must be [kv_heads][num_pages*page_size][head_dim], got {tuple(K.shape)}")
+        self.K, self.V, self.cfg = K, V, c
+        self.num_pages = K.shape[1] // c.page_size
+        self.handle = pkv_pool_wrap(c, self.num_pages, K, V, stream)
+        self._ws = None
+
+    def workspace(self, rows: int, pages: int, prefill_tokens: int = 0) -> torch.Tensor:
+        n = pkv_workspace_bytes(self.handle, rows, pages, prefill_tokens)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.K.device)
+        return self._ws
+
+    def decode(self, q, k, v, q_norm_w, k_norm_w, positions, table, out=None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(table.shape[0], table.shape[1], 0)
+        pkv_decode(self.handle, q, k, v, q_norm_w, k_norm_w, positions, table, out, ws, stream)
+        return out
+
+    def step(self, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out=None,
+             stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(table.shape[0], table.shape[1], positions.shape[0])
+        pkv_step(self.handle, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out, ws,
+                 stream)
+        return out
+
+    def check_errors(self, stream=None) -> int:
+        return pkv_check_errors(self.handle, stream)
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            pkv_pool_free(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

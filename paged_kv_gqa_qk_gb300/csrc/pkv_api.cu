@@ -1,0 +1,402 @@
+// Host side of libpkv: the C ABI declared in include/pkv.h.
+//
+// pkv_decode / pkv_step validate their arguments on the host, carve the
+// caller's workspace, and enqueue three kernels on the caller's stream:
+//   prep (QK-norm + RoPE + append) -> split-KV attention -> split combine.
+// The second and third use programmatic dependent launch so their prologues
+// overlap the tail of the kernel before them.  Nothing here allocates or
+// synchronises on the call path.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Pages per split.  The split-KV grid is (tokens x kv_heads x max_splits)
+// CTAs; a split covers `chunk` pages of the table's width.  Aim for several
+// waves of two resident CTAs per SM over the widest possible rows, with
+// splits of at most 32 pages (512 KiB of K+V per kv head).
+static int auto_chunk(const pkv_pool* pool, int tokens, int pages)
+{
+    const int64_t units = (int64_t)tokens * pool->cfg.kv_heads;
+    const int64_t total = units * pages;
+    const int64_t target = (int64_t)pool->num_sms * 2 * 6;
+    int64_t chunk = (total + target - 1) / target;
+    if (chunk < 1) chunk = 1;
+    if (chunk > 32) chunk = 32;
+    return (int)chunk;
+}
+
+Plan make_plan(const pkv_pool* pool, int tokens, int pages)
+{
+    Plan pl;
+    pl.tokens = tokens;
+    pl.pages = pages;
+    pl.chunk = pool->split_pages > 0 ? pool->split_pages : auto_chunk(pool, tokens, pages);
+    if (pl.chunk > pages) pl.chunk = pages;
+    pl.max_splits = (pages + pl.chunk - 1) / pl.chunk;
+    const size_t H = (size_t)pool->cfg.heads, D = (size_t)pool->cfg.head_dim;
+    size_t off = 0;
+    pl.off_len = off;
+    off = align_up(off + sizeof(int32_t) * tokens, 256);
+    pl.off_row = off;
+    off = align_up(off + sizeof(int32_t) * tokens, 256);
+    pl.off_qhat = off;
+    off = align_up(off + sizeof(float) * tokens * H * D, 256);
+    if (pl.max_splits > 1) {
+        pl.off_po = off;
+        off = align_up(off + sizeof(float) * tokens * H * pl.max_splits * D, 256);
+        pl.off_plse = off;
+        off = align_up(off + sizeof(float) * tokens * H * pl.max_splits, 256);
+    } else {
+        pl.off_po = pl.off_plse = 0;
+    }
+    pl.total = off;
+    return pl;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 3-D tiled view {head_dim, num_slots, kv_heads} of one pool tensor; a box is
+// 64 head-dim elements (128 bytes, the swizzle span) x 64 slots (one page).
+static bool make_tmap(CUtensorMap* map, void* base, int64_t num_slots, int kv_heads)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_slots, (cuuint64_t)kv_heads};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)num_slots * kHeadDim * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kPageSize, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int check_config(const pkv_config* c)
+{
+    if (c->heads <= 0 || c->kv_heads <= 0 || c->head_dim <= 0 || c->page_size <= 0 || c->max_seq <= 0)
+        return PKV_EINVAL;
+    if (c->heads % c->kv_heads != 0 || c->head_dim % 2 != 0) return PKV_EINVAL;
+    if (!(c->rope_theta > 0.0) || !(c->eps >= 0.0) || !std::isfinite(c->rope_theta) || !std::isfinite(c->eps))
+        return PKV_EINVAL;
+    if (c->head_dim != kHeadDim || c->page_size != kPageSize || c->heads != kGroup * c->kv_heads)
+        return PKV_ENOTIMPL;
+    if (c->max_seq > (1 << 20) || c->kv_heads > 256) return PKV_ERANGE;
+    return PKV_OK;
+}
+
+// RoPE table: (cos, sin) of pos * theta^(-2i/head_dim), i < head_dim/2, for
+// every position < max_seq, in double precision (qwen3-8b Nest files,
+// src/rope.linnet tables; the pages evaluate the angle in f32, which at
+// position 40959 is off by up to ~2e-3 rad).  The k rotation uses it in
+// double so the written K is within one rounding of the exact value even when
+// the two rotated terms cancel; q uses it rounded to fp32.
+static void rope_table(const pkv_config& c, std::vector<double2>& cs)
+{
+    const int half = c.head_dim / 2;
+    cs.resize((size_t)c.max_seq * half);
+    std::vector<double> inv(half);
+    for (int i = 0; i < half; ++i) inv[i] = std::pow(c.rope_theta, -2.0 * i / (double)c.head_dim);
+    for (int p = 0; p < c.max_seq; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double a = (double)p * inv[i];
+            cs[(size_t)p * half + i] = make_double2(std::cos(a), std::sin(a));
+        }
+}
+
+static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, bool owns, void* stream,
+                       pkv_pool** out)
+{
+    if (!cfg || !out || num_pages <= 0) return PKV_EINVAL;
+    *out = nullptr;
+    int rc = check_config(cfg);
+    if (rc != PKV_OK) return rc;
+    const int64_t num_slots = (int64_t)num_pages * cfg->page_size;
+    if (num_slots >= (int64_t(1) << 31)) return PKV_ERANGE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_EDEVICE;
+    int major = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major < 10 || sms <= 0) return PKV_EDEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    pkv_pool* p = new (std::nothrow) pkv_pool();
+    if (!p) return PKV_ENOMEM;
+    p->cfg = *cfg;
+    p->device = dev;
+    p->num_sms = sms;
+    p->num_pages = num_pages;
+    p->num_slots = num_slots;
+    p->owns_kv = owns;
+    const size_t kv_bytes = (size_t)cfg->kv_heads * num_slots * cfg->head_dim * 2;
+    const size_t tab = (size_t)cfg->max_seq * (cfg->head_dim / 2) * sizeof(double2);
+    bool fail = false;
+    if (owns) {
+        fail |= cudaMalloc(&p->k, kv_bytes) != cudaSuccess;
+        fail |= !fail && cudaMalloc(&p->v, kv_bytes) != cudaSuccess;
+    } else {
+        p->k = k;
+        p->v = v;
+    }
+    fail |= !fail && cudaMalloc(reinterpret_cast<void**>(&p->rope), tab) != cudaSuccess;
+    fail |= !fail && cudaMalloc(reinterpret_cast<void**>(&p->err), 256) != cudaSuccess;
+    if (fail) {
+        cudaGetLastError();
+        pkv_pool_free(p);
+        return PKV_ENOMEM;
+    }
+    std::vector<double2> cs;
+    rope_table(*cfg, cs);
+    bool ok = true;
+    if (owns) {
+        ok &= cudaMemsetAsync(p->k, 0, kv_bytes, s) == cudaSuccess;
+        ok &= cudaMemsetAsync(p->v, 0, kv_bytes, s) == cudaSuccess;
+    }
+    ok &= cudaMemcpyAsync(p->rope, cs.data(), tab, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    ok &= cudaMemsetAsync(p->err, 0, 256, s) == cudaSuccess;
+    ok &= cudaStreamSynchronize(s) == cudaSuccess;  // the host vectors die with this call
+    ok &= make_tmap(&p->tmap_k, p->k, num_slots, cfg->kv_heads);
+    ok &= make_tmap(&p->tmap_v, p->v, num_slots, cfg->kv_heads);
+    ok &= configure_kernels() == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        pkv_pool_free(p);
+        return PKV_ECUDA;
+    }
+    *out = p;
+    return PKV_OK;
+}
+
+static bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+static int run_step(pkv_pool* pool, const StepArgs& a0, size_t ws_bytes, void* stream)
+{
+    StepArgs a = a0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    const int tokens = a.P + a.rows;
+    Plan plan = make_plan(pool, tokens, a.pages);
+    if (!a.ws || ws_bytes < plan.total) return PKV_EWORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_prep(pool, a, plan, s);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    const bool timed = pool->timer_on;
+    const int slot = (int)(pool->timer_count % kTimerSlots);
+    if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
+    e = launch_attn_decode(pool, a, plan, s);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    if (timed) {
+        if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
+        pool->timer_count++;
+    }
+    e = launch_combine(pool, a, plan, s);
+    if (e != cudaSuccess) return PKV_ECUDA;
+    return PKV_OK;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_config_default(pkv_config* cfg)
+{
+    if (!cfg) return PKV_EINVAL;
+    cfg->heads = 32;
+    cfg->kv_heads = 8;
+    cfg->head_dim = 128;
+    cfg->page_size = 64;
+    cfg->max_seq = 40960;
+    cfg->rope_theta = 1.0e6;
+    cfg->eps = 1.0e-6;
+    return PKV_OK;
+}
+
+const char* pkv_strerror(int code)
+{
+    switch (code) {
+        case PKV_OK: return "ok";
+        case PKV_EINVAL: return "invalid argument";
+        case PKV_ERANGE: return "size out of supported range";
+        case PKV_ENOMEM: return "device allocation failed";
+        case PKV_ECUDA: return "CUDA runtime error";
+        case PKV_EWORKSPACE: return "workspace too small";
+        case PKV_EDEVICE: return "no usable device or wrong device";
+        case PKV_ENOTIMPL: return "configuration not supported by the kernels";
+        default: return "unknown error";
+    }
+}
+
+int pkv_pool_alloc(const pkv_config* cfg, int num_pages, void* stream, pkv_pool** out)
+{
+    return create_pool(cfg, num_pages, nullptr, nullptr, true, stream, out);
+}
+
+int pkv_pool_wrap(const pkv_config* cfg, int num_pages, void* k, void* v, void* stream, pkv_pool** out)
+{
+    if (!k || !v || !aligned(k, 256) || !aligned(v, 256)) return PKV_EINVAL;
+    return create_pool(cfg, num_pages, k, v, false, stream, out);
+}
+
+int pkv_pool_free(pkv_pool* p)
+{
+    if (!p) return PKV_OK;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(p->device);
+    cudaDeviceSynchronize();
+    if (p->owns_kv) {
+        if (p->k) cudaFree(p->k);
+        if (p->v) cudaFree(p->v);
+    }
+    if (p->rope) cudaFree(p->rope);
+    if (p->err) cudaFree(p->err);
+    if (p->ev_start) {
+        for (int i = 0; i < kTimerSlots; ++i) {
+            cudaEventDestroy(p->ev_start[i]);
+            cudaEventDestroy(p->ev_stop[i]);
+        }
+        delete[] p->ev_start;
+        delete[] p->ev_stop;
+    }
+    if (prev >= 0) cudaSetDevice(prev);
+    delete p;
+    return PKV_OK;
+}
+
+int pkv_pool_kv(const pkv_pool* pool, void** k, void** v, int64_t* num_slots)
+{
+    if (!pool) return PKV_EINVAL;
+    if (k) *k = pool->k;
+    if (v) *v = pool->v;
+    if (num_slots) *num_slots = pool->num_slots;
+    return PKV_OK;
+}
+
+int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_tokens, size_t* bytes)
+{
+    if (!pool || !bytes || rows < 0 || prefill_tokens < 0 || rows + prefill_tokens <= 0 || pages <= 0)
+        return PKV_EINVAL;
+    if ((int64_t)rows + prefill_tokens > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    *bytes = make_plan(pool, rows + prefill_tokens, pages).total;
+    return PKV_OK;
+}
+
+int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+               const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows, int pages,
+               void* out, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !table || !out) return PKV_EINVAL;
+    if (rows <= 0 || pages <= 0) return PKV_EINVAL;
+    if (rows > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
+        !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(table, 4))
+        return PKV_EINVAL;
+    if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
+    StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
+                  0, rows, pages, out, static_cast<char*>(workspace)};
+    return run_step(pool, a, workspace_bytes, stream);
+}
+
+int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+             const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
+             const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
+             void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !prow || !step_positions || !table ||
+        !out)
+        return PKV_EINVAL;
+    if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
+    if ((int64_t)P + rows > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
+        !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(prow, 4) || !aligned(step_positions, 4) ||
+        !aligned(table, 4) || (slots && !aligned(slots, 4)))
+        return PKV_EINVAL;
+    if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
+    StepArgs a = {q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table,
+                  P, rows, pages, out, static_cast<char*>(workspace)};
+    return run_step(pool, a, workspace_bytes, stream);
+}
+
+int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags)
+{
+    if (!pool || !flags) return PKV_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ECUDA;
+    uint32_t h = 0;
+    if (cudaMemcpy(&h, pool->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ECUDA;
+    if (cudaMemset(pool->err, 0, sizeof h) != cudaSuccess) return PKV_ECUDA;
+    *flags = h;
+    return PKV_OK;
+}
+
+int pkv_set_split_pages(pkv_pool* pool, int pages_per_split)
+{
+    if (!pool || pages_per_split < 0) return PKV_EINVAL;
+    pool->split_pages = pages_per_split;
+    return PKV_OK;
+}
+
+int pkv_timer_enable(pkv_pool* pool, int enable)
+{
+    if (!pool) return PKV_EINVAL;
+    if (enable && !pool->ev_start) {
+        pool->ev_start = new (std::nothrow) cudaEvent_t[kTimerSlots];
+        pool->ev_stop = new (std::nothrow) cudaEvent_t[kTimerSlots];
+        if (!pool->ev_start || !pool->ev_stop) return PKV_ENOMEM;
+        for (int i = 0; i < kTimerSlots; ++i) {
+            if (cudaEventCreate(&pool->ev_start[i]) != cudaSuccess ||
+                cudaEventCreate(&pool->ev_stop[i]) != cudaSuccess)
+                return PKV_ECUDA;
+        }
+    }
+    pool->timer_on = enable != 0;
+    pool->timer_count = 0;
+    return PKV_OK;
+}
+
+int pkv_timer_read(pkv_pool* pool, double* total_ms, int64_t* launches)
+{
+    if (!pool || !total_ms || !launches) return PKV_EINVAL;
+    *total_ms = 0.0;
+    *launches = 0;
+    if (!pool->ev_start || pool->timer_count == 0) return PKV_OK;
+    const int64_t n = pool->timer_count < kTimerSlots ? pool->timer_count : kTimerSlots;
+    const int last = (int)((pool->timer_count - 1) % kTimerSlots);
+    if (cudaEventSynchronize(pool->ev_stop[last]) != cudaSuccess) return PKV_ECUDA;
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int sl = (int)((pool->timer_count - 1 - i) % kTimerSlots);
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, pool->ev_start[sl], pool->ev_stop[sl]) != cudaSuccess) return PKV_ECUDA;
+        sum += ms;
+    }
+    *total_ms = sum;
+    *launches = n;
+    return PKV_OK;
+}
+
+}  // extern "C"

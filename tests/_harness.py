@@ -1,0 +1,88 @@
+"""Shared helpers for the GPU parity tests: run a workload through the C ABI
+and through the fp64 oracle, and compare them element by element."""
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_gqa_qk_gb300 as pkv
+import workloads as W
+
+# Output tolerances against the oracle's fp64 values (max-abs and relative L2).
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+
+
+def run_gpu(wl: W.Workload, split_pages: int = 0, explicit_slots=None, table=None, step_positions=None,
+            positions=None, repeat: int = 1):
+    dev = torch.device("cuda")
+    K, V = wl.K0.to(dev), wl.V0.to(dev)
+    pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+    if split_pages:
+        pkv.pkv_set_split_pages(pool.handle, split_pages)
+    q, k, v, qw, kw = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w))
+    tab = (wl.table if table is None else torch.as_tensor(table)).to(dev)
+    sp = (wl.step_positions if step_positions is None else torch.as_tensor(step_positions)).to(dev)
+    for _ in range(repeat):
+        if wl.kind == "decode":
+            out = pool.decode(q, k, v, qw, kw, sp, tab)
+        else:
+            pos = (wl.positions if positions is None else torch.as_tensor(positions)).to(dev)
+            slots = None if explicit_slots is None else torch.as_tensor(explicit_slots, dtype=torch.int32).to(dev)
+            out = pool.step(q, k, v, qw, kw, pos, wl.prow.to(dev), slots, sp, tab)
+    flags = pool.check_errors()
+    res = (out.cpu(), K.cpu(), V.cpu(), flags)
+    pool.close()
+    return res
+
+
+def run_oracle(wl: W.Workload, sel=None, table=None, step_positions=None, positions=None):
+    K, V = W.bits(wl.K0).copy(), W.bits(wl.V0).copy()
+    args = [W.bits(t) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w)]
+    tab = (wl.table if table is None else torch.as_tensor(table)).numpy()
+    sp = (wl.step_positions if step_positions is None else torch.as_tensor(step_positions)).numpy()
+    if wl.kind == "decode":
+        out, err = oracle.decode(K, V, *args, sp, tab, cfg=wl.cfg, sel=sel)
+    else:
+        pos = (wl.positions if positions is None else torch.as_tensor(positions)).numpy()
+        out, err = oracle.step(K, V, *args, pos, wl.prow.numpy(), None, sp, tab, cfg=wl.cfg, sel=sel)
+    return out, K, V, err
+
+
+def ulp_distance_bf16(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in bf16 ulps between two arrays of bf16 bit patterns (uint16)."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, 0x8000 - x, x)   # monotone map of bf16 bits to integers
+    return np.abs(ordered(a) - ordered(b))
+
+
+def compare(wl, gpu, ref, sel=None, label=""):
+    """Assert the GPU result matches the oracle; returns (max_abs, rel_l2)."""
+    out, K, V, flags = gpu
+    rout, rK, rV, rerr = ref
+    assert flags == rerr, f"{label}: device error bits {flags} != oracle {rerr}"
+    Kb, Vb = W.bits(K), W.bits(V)
+    K0 = W.bits(wl.K0)
+    # V: bit-exact everywhere (written slots and untouched entries)
+    assert np.array_equal(Vb, rV), f"{label}: V pool differs from the oracle"
+    # K: untouched entries bit-exact, written entries within 1 bf16 ulp
+    written = np.any(rK != K0, axis=-1) | np.any(Kb != K0, axis=-1)
+    assert np.array_equal(Kb[~written], rK[~written]), f"{label}: untouched K entries changed"
+    if written.any():
+        d = ulp_distance_bf16(Kb[written], rK[written])
+        if d.max() > 1:
+            i = np.unravel_index(np.argmax(d), d.shape)
+            gv = oracle.bf16_to_f64(Kb[written][i])
+            rv = oracle.bf16_to_f64(rK[written][i])
+            raise AssertionError(f"{label}: written K off by {d.max()} ulp ({(d > 1).sum()} elements > 1 ulp); "
+                                 f"worst: gpu {gv!r} oracle {rv!r}, row max |k| "
+                                 f"{np.abs(oracle.bf16_to_f64(rK[written][i[0]])).max():.3f}")
+    got = out.float().double().numpy()
+    if sel is not None:
+        got, rout = got[sel], rout[sel]
+    max_abs = float(np.abs(got - rout).max()) if got.size else 0.0
+    nrm = float(np.linalg.norm(rout))
+    rel = float(np.linalg.norm(got - rout) / nrm) if nrm > 0 else float(np.linalg.norm(got))
+    assert max_abs <= MAX_ABS, f"{label}: max-abs {max_abs:.3e} > {MAX_ABS}"
+    assert rel <= REL_L2, f"{label}: rel-L2 {rel:.3e} > {REL_L2}"
+    return max_abs, rel

@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs.
+
+Bar (per output element / pool entry):
+  * page/slot placement and untouched pool entries bit-exact, V bit-exact,
+    written K within 1 bf16 ulp of the oracle's correctly rounded value;
+  * attention outputs within max-abs 2e-2 and relative-L2 5e-3 of the
+    oracle's fp64 result;
+  * device error bits equal to the oracle's skip reasons.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_qk_gb300 as pkv
+import workloads as W
+from _harness import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ the five configurations
+
+@pytest.mark.parametrize("split", [0, 1, 2])
+def test_config1_tiny(split):
+    wl = W.config1()
+    ma, rel = compare(wl, run_gpu(wl, split_pages=split), run_oracle(wl), label=f"config1 split={split}")
+    assert ma < 5e-3
+
+
+def test_config2_decode_64_rows():
+    wl = W.config2()
+    compare(wl, run_gpu(wl), run_oracle(wl), label="config2")
+
+
+def test_config3_long_context():
+    wl = W.config3()
+    compare(wl, run_gpu(wl), run_oracle(wl), label="config3")
+
+
+def test_config4_shared_prefixes():
+    wl = W.config4()
+    compare(wl, run_gpu(wl), run_oracle(wl), label="config4")
+
+
+def test_config5_step_mix():
+    wl = W.config5()
+    # all decode rows, and a sample of prompt tokens: every 16th plus each
+    # prompt's first and last token
+    P = wl.P
+    starts = np.cumsum([0] + wl.meta["prompt_lengths"])
+    sel = sorted(set(range(0, P, 16)) | set(starts[:-1].tolist()) | set((starts[1:] - 1).tolist())
+                 | set(range(P, P + wl.R)))
+    compare(wl, run_gpu(wl), run_oracle(wl, sel=sel), sel=sel, label="config5")
+
+
+# ------------------------------------------------------------------ tiles, ragged tails, split sizes
+
+RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 191, 640, 1000, 4097]
+
+
+@pytest.mark.parametrize("split", [0, 1, 3, 7])
+def test_ragged_lengths_and_split_sizes(split):
+    wl = W.make_decode("ragged", RAGGED, seed=77, table_pages=70)
+    compare(wl, run_gpu(wl, split_pages=split), run_oracle(wl), label=f"ragged split={split}")
+
+
+def test_sweep_shape_small():
+    wl = W.sweep(8, 4096, seed=5)
+    compare(wl, run_gpu(wl), run_oracle(wl), label="sweep 8x4096")
+
+
+def test_step_small_with_explicit_slots():
+    wl = W.make_step("small step", prompt_lengths=[70, 5, 130], prompt_starts=[60, 0, 500],
+                     decode_lengths=[90, 3, 64, 65, 1], seed=21, table_pages=12)
+    slots = oracle.page_slots(wl.table.numpy(), wl.prow.numpy(), wl.positions.numpy())
+    ref = run_oracle(wl)
+    compare(wl, run_gpu(wl, explicit_slots=slots), ref, label="step explicit slots")
+    compare(wl, run_gpu(wl), ref, label="step derived slots")
+    compare(wl, run_gpu(wl, split_pages=1), ref, label="step split=1")
+
+
+def test_repeated_calls_are_idempotent():
+    wl = W.make_decode("repeat", [300, 5, 1000], seed=22, table_pages=16)
+    compare(wl, run_gpu(wl, repeat=3), run_oracle(wl), label="repeat x3")
+
+
+# ------------------------------------------------------------------ skipped tokens and device errors
+
+def test_inactive_and_invalid_rows():
+    wl = W.make_decode("errors", [100, 70, 5, 2000, 64], seed=23, table_pages=32)
+    sp = wl.step_positions.clone()
+    table = wl.table.clone()
+    sp[0] = -1                       # no step: zero output, no write, no error
+    sp[1] = 40960                    # beyond max_seq
+    table[2, 0] = wl.num_pages + 7   # not a pool page
+    sp[4] = 32 * 64                  # beyond the table width
+    gpu = run_gpu(wl, table=table, step_positions=sp)
+    ref = run_oracle(wl, table=table, step_positions=sp)
+    assert ref[3] == (oracle.ERR_POSITION | oracle.ERR_PAGE)
+    compare(wl, gpu, ref, label="errors")
+    out = gpu[0]
+    for b in (0, 1, 2, 4):
+        assert not out[b].float().abs().sum()
+
+
+def test_step_invalid_prompt_tokens():
+    wl = W.make_step("step errors", prompt_lengths=[40, 30], prompt_starts=[0, 100], decode_lengths=[50, 10],
+                     seed=24, table_pages=4)
+    pos = wl.positions.clone()
+    pos[3] = -5                      # negative position
+    gpu_prow = wl.prow.clone()
+    prow_bad = gpu_prow.clone()
+    prow_bad[10] = 99                # row outside the table
+    wl_bad = W.Workload(**{**wl.__dict__, "prow": prow_bad})
+    gpu = run_gpu(wl_bad, positions=pos)
+    ref = run_oracle(wl_bad, positions=pos)
+    assert ref[3] == (oracle.ERR_POSITION | oracle.ERR_ROW)
+    compare(wl_bad, gpu, ref, label="step errors")
+
+
+def test_host_errors_enqueue_nothing():
+    wl = W.config1()
+    dev = torch.device("cuda")
+    K, V = wl.K0.to(dev), wl.V0.to(dev)
+    pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+    q, k, v, qw, kw, sp, tab = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w,
+                                                   wl.step_positions, wl.table))
+    out = torch.zeros_like(q)
+    need = pkv.pkv_workspace_bytes(pool.handle, 2, 2, 0)
+    small = torch.empty(need - 256, dtype=torch.uint8, device=dev)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_decode(pool.handle, q, k, v, qw, kw, sp, tab, out, small)
+    assert ei.value.code == pkv.PKV_EWORKSPACE
+    torch.cuda.synchronize()
+    assert not out.any()
+    assert torch.equal(K.cpu(), wl.K0) and torch.equal(V.cpu(), wl.V0)
+    # unsupported shapes are refused at pool creation
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_pool_alloc(dict(wl.cfg, head_dim=64), 4)
+    assert ei.value.code == pkv.PKV_ENOTIMPL
+    pool.close()
+
+
+def test_pool_alloc_owns_zeroed_memory():
+    cfg = pkv.pkv_config_default()
+    pool = pkv.pkv_pool_alloc(cfg, 3)
+    k, v, n = pkv.pkv_pool_kv(pool)
+    assert n == 3 * 64 and k and v and k % 256 == 0
+    pkv.pkv_pool_free(pool)
+
+
+# ------------------------------------------------------------------ partition by kv heads
+
+def test_kv_head_shards_reproduce_full_result():
+    """The attention needs no exchange between kv-head groups: running the
+    library once per kv-head shard (a pool of kv_heads/n heads, the matching
+    query heads) and concatenating reproduces the full result bit-exactly."""
+    wl = W.make_decode("shard", [500, 64, 1300, 7], seed=25, table_pages=24)
+    full = run_gpu(wl, split_pages=4)
+    n = 4
+    G = wl.cfg["kv_heads"] // n
+    outs = []
+    for r in range(n):
+        g0, g1 = r * G, (r + 1) * G
+        cfg = dict(wl.cfg, kv_heads=G, heads=4 * G)
+        part = W.Workload(wl.name, cfg, wl.num_pages, wl.K0[g0:g1].contiguous(), wl.V0[g0:g1].contiguous(),
+                          wl.q[:, 4 * g0:4 * g1].contiguous(), wl.k[:, g0:g1].contiguous(),
+                          wl.v[:, g0:g1].contiguous(), wl.q_norm_w, wl.k_norm_w, wl.table, wl.step_positions)
+        out, K, V, flags = run_gpu(part, split_pages=4)
+        assert flags == 0
+        assert torch.equal(K, full[1][g0:g1]) and torch.equal(V, full[2][g0:g1])
+        outs.append(out)
+    assert torch.equal(torch.cat(outs, dim=1), full[0])
