@@ -200,6 +200,34 @@ PKV_API int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v
              const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
              void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- decode without a caller workspace -------------------------------------------------------
+ * The pages have no counterpart to this entry point; it is a convenience of
+ * this library.  It is pkv_decode for callers that cannot allocate device
+ * memory at all: for example a plug-in whose host application owns every
+ * device allocation and hands it none, or a process whose device memory is
+ * reserved in full up front by another allocator, where one more cudaMalloc
+ * would fail, or would stall the whole device while it runs.
+ *
+ * Instead of a caller workspace it uses a scratch array compiled into the
+ * library: PKV_STATIC_SCRATCH_BYTES (32 MiB) of device memory that every GPU
+ * that loads the library holds until the process exits.  The call itself
+ * allocates nothing.  The caller still passes the pool, inputs and output,
+ * exactly as for pkv_decode (same layouts, same error codes), minus the
+ * workspace.
+ *   - The first call on each device looks up the array's device address, with
+ *     that device current.  Make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero.  Calls whose work overlaps on the
+ *     GPU (e.g. on two streams with no ordering between them) race on the array
+ *     and their results are undefined.
+ *   - A call that needs more scratch than the array holds (more than
+ *     PKV_STATIC_SCRATCH_BYTES from pkv_workspace_bytes(pool, rows, pages, 0))
+ *     is rejected with PKV_ERANGE and nothing is enqueued. */
+#define PKV_STATIC_SCRATCH_BYTES (32u << 20)
+PKV_API int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+                              const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows,
+                              int pages, void* out, void* stream);
+
 /* ---- errors ------------------------------------------------------------------------------
  * Synchronise `stream`, then read and clear the pool's sticky device error
  * word (PKV_DEVERR_* bits of every call since the last read) into *flags.

@@ -26,7 +26,10 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 # Every symbol include/pkv.h declares.
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
                "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_check_errors",
-               "pkv_set_split_pages", "pkv_timer_enable", "pkv_timer_read")
+               "pkv_set_split_pages", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static")
+
+# Size of the scratch array pkv_decode_static uses in place of a workspace.
+PKV_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class PkvConfig(ctypes.Structure):
@@ -72,6 +75,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_set_split_pages": ([vp, i32], i32),
         "pkv_timer_enable": ([vp, i32], i32),
         "pkv_timer_read": ([vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)], i32),
+        "pkv_decode_static": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -173,6 +177,16 @@ def pkv_decode(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, workspa
         _dev(positions, torch.int32, "positions"), _dev(table, torch.int32, "table"), rows, pages,
         _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), _stream(stream)), "pkv_decode")
+
+
+def pkv_decode_static(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, stream=None) -> None:
+    """pkv_decode without a workspace: the library's static scratch array is used instead."""
+    rows, pages = int(table.shape[0]), int(table.shape[1])
+    _check(load_library().pkv_decode_static(
+        pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
+        _dev(positions, torch.int32, "positions"), _dev(table, torch.int32, "table"), rows, pages,
+        _dev(out, torch.bfloat16, "out"), _stream(stream)), "pkv_decode_static")
 
 
 def pkv_step(pool, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out, workspace,

@@ -1,0 +1,68 @@
+// pkv_decode_static: decode_paged for callers that cannot allocate device
+// memory.  The scratch that pkv_decode takes from the caller's workspace comes
+// from a fixed array compiled into this file instead; the call allocates
+// nothing and otherwise runs the same three kernels as pkv_decode.
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace {
+
+// The library's own scratch: every GPU that loads libpkv holds it until the
+// process exits.  Its contents persist between calls (they need no zeroing:
+// every call writes each scratch entry it reads).
+__device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device; null until set up
+
+// Device address of the scratch array on `dev` (the current device).  Looked
+// up once per device, on that device's first call.
+int scratch_address(int dev, void** out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return PKV_EDEVICE;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return PKV_ECUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return PKV_OK;
+}
+
+bool aligned_to(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+}  // namespace
+
+extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+                                 const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows,
+                                 int pages, void* out, void* stream)
+{
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !table || !out) return PKV_EINVAL;
+    if (rows <= 0 || pages <= 0) return PKV_EINVAL;
+    if (rows > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned_to(q, 8) || !aligned_to(k, 8) || !aligned_to(v, 8) || !aligned_to(out, 8) ||
+        !aligned_to(q_norm_w, 8) || !aligned_to(k_norm_w, 8) || !aligned_to(positions, 4) || !aligned_to(table, 4))
+        return PKV_EINVAL;
+    const pkv::Plan plan = pkv::make_plan(pool, rows, pages);
+    if (plan.total > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERANGE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    void* scratch = nullptr;
+    const int rc = scratch_address(dev, &scratch);
+    if (rc != PKV_OK) return rc;
+
+    pkv::StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
+                       0, rows, pages, out, static_cast<char*>(scratch)};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pkv::launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+    if (pkv::launch_attn_decode(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+    if (pkv::launch_combine(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+    return PKV_OK;
+}
