@@ -105,9 +105,10 @@ PKV_API const char* pkv_strerror(int code);
  * ((g * num_pages + p) * page_size + s) * head_dim.  For one kv head a page is
  * one contiguous block of page_size * head_dim * 2 bytes (16 KiB).
  *
- * A pool also holds the RoPE (cos, sin) table for positions 0..max_seq-1
- * (double precision, computed on the host; 16 bytes x head_dim/2 x max_seq,
- * 42 MB at the defaults) and the sticky device error word. */
+ * A pool also holds the RoPE (cos, sin) tables for positions 0..max_seq-1
+ * (computed on the host in double precision and kept as fp32 hi + lo parts;
+ * 16 bytes x head_dim/2 x max_seq, 42 MB at the defaults) and the sticky
+ * device error word. */
 typedef struct pkv_pool pkv_pool;
 
 /* Create a pool that owns num_pages pages of K and V on the current device
@@ -139,9 +140,11 @@ PKV_API int pkv_pool_kv(const pkv_pool* pool, void** k, void** v, int64_t* num_s
  * rows` tokens and a page table `pages` wide.  The caller allocates it (256-byte
  * aligned) and passes it to pkv_decode / pkv_step; its contents need no
  * initialisation and are not meaningful after the call.  The size depends
- * only on (pool config, rows, pages, prefill_tokens).
+ * only on the pool (its config and attention grid size, see pkv_set_ctas),
+ * rows and prefill_tokens: about 16.5 KiB per token plus 2 KiB per attention
+ * CTA.
  * Errors: PKV_EINVAL (null, rows < 0, prefill_tokens < 0, both zero,
- * pages <= 0), PKV_ERANGE (too many tokens). */
+ * pages <= 0), PKV_ERANGE (more than 2^20 tokens). */
 PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_tokens, size_t* bytes);
 
 /* ---- decode_paged ------------------------------------------------------------------
@@ -153,7 +156,8 @@ PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int p
  * through table[b] (so it sees its own new key).  All writes of the call
  * happen before any attention.
  *
- *   q         device bf16 [rows][heads][head_dim]     (projected, split into heads)
+ *   q         device bf16 [rows][heads][head_dim]     (projected, split into heads;
+ *             16-byte aligned: its head groups are bulk-copied)
  *   k, v      device bf16 [rows][kv_heads][head_dim]
  *   q_norm_w  device bf16 [head_dim]                  (QK-norm weights)
  *   k_norm_w  device bf16 [head_dim]
@@ -167,6 +171,10 @@ PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int p
  *
  * Slots written by one call must be distinct (the pages' write_tokens is a
  * scatter); if two tokens write one slot, which value lands is unspecified.
+ * A row's new slot must not be read by another row of the same call (rows
+ * may share pages, but only pages before their own write page, as a
+ * shared prompt prefix is): each row's write is ordered before its own read,
+ * not before other rows' reads.  pkv_step has no such condition.
  * Returns PKV_OK once the work is enqueued, or a PKV_E* code with nothing
  * enqueued. */
 PKV_API int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
@@ -184,7 +192,7 @@ PKV_API int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void*
  * 0..positions[p] (its own chunk's earlier keys included), and row b over
  * 0..step_positions[b].
  *
- *   q              device bf16 [P + rows][heads][head_dim]
+ *   q              device bf16 [P + rows][heads][head_dim], 16-byte aligned
  *   k, v           device bf16 [P + rows][kv_heads][head_dim]
  *   positions      device int32 [P]
  *   prow           device int32 [P]    (the pages' `rows` argument)
@@ -193,8 +201,9 @@ PKV_API int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void*
  *   table          device int32 [rows][pages]
  *   out            device bf16 [P + rows][heads][head_dim] (prompts, then steps)
  *   workspace      >= pkv_workspace_bytes(pool, rows, pages, P)
- * The pages require P > 0 and rows > 0 (PKV_EINVAL otherwise).  Slot
- * uniqueness as for pkv_decode. */
+ * The pages require P > 0 and rows > 0 (PKV_EINVAL otherwise).  Slots must
+ * be distinct as for pkv_decode; every write of the call is ordered before
+ * every read. */
 PKV_API int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
              const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
              const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
@@ -235,14 +244,15 @@ PKV_API int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, cons
 PKV_API int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags);
 
 /* ---- tuning and measurement ---------------------------------------------------------------
- * Pages each split of the split-KV attention covers (0 = automatic, chosen
- * from the SM count, rows and table width).  Results do not depend on it
- * beyond floating-point association.  Errors: PKV_EINVAL (null, < 0). */
-PKV_API int pkv_set_split_pages(pkv_pool* pool, int pages_per_split);
+ * Grid size of the attention kernel (0 = one wave: every SM's resident
+ * CTAs).  The kernel splits the call's (token, kv head, page) sequence into
+ * that many equal slices; results do not depend on it beyond floating-point
+ * association.  It changes pkv_workspace_bytes.  Errors: PKV_EINVAL (null, < 0). */
+PKV_API int pkv_set_ctas(pkv_pool* pool, int ctas);
 
 /* Kernel timer: while enabled, every pkv_decode / pkv_step records a pair of
- * CUDA events on its stream around the split-KV attention kernel (the
- * dominant launch).  pkv_timer_read synchronises on the last recorded event,
+ * CUDA events on its stream around the attention kernel (the dominant
+ * launch).  pkv_timer_read synchronises on the last recorded event,
  * returns the summed duration in milliseconds and the number of timed
  * launches since the timer was last enabled, and keeps the timer running.
  * At most 4096 launches are kept (later ones overwrite the oldest). */

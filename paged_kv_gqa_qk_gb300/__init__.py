@@ -26,7 +26,7 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 # Every symbol include/pkv.h declares.
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
                "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_check_errors",
-               "pkv_set_split_pages", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static")
+               "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static")
 
 # Size of the scratch array pkv_decode_static uses in place of a workspace.
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
@@ -72,7 +72,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_decode": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp], i32),
         "pkv_step": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp], i32),
         "pkv_check_errors": ([vp, vp, ctypes.POINTER(ctypes.c_uint32)], i32),
-        "pkv_set_split_pages": ([vp, i32], i32),
+        "pkv_set_ctas": ([vp, i32], i32),
         "pkv_timer_enable": ([vp, i32], i32),
         "pkv_timer_read": ([vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)], i32),
         "pkv_decode_static": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp], i32),
@@ -208,8 +208,8 @@ def pkv_check_errors(pool, stream=None) -> int:
     return f.value
 
 
-def pkv_set_split_pages(pool, pages_per_split: int) -> None:
-    _check(load_library().pkv_set_split_pages(pool, int(pages_per_split)), "pkv_set_split_pages")
+def pkv_set_ctas(pool, ctas: int) -> None:
+    _check(load_library().pkv_set_ctas(pool, int(ctas)), "pkv_set_ctas")
 
 
 def pkv_timer_enable(pool, enable: bool) -> None:

@@ -20,47 +20,52 @@ namespace pkv {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Pages per split.  The split-KV grid is (tokens x kv_heads x max_splits)
-// CTAs; a split covers `chunk` pages of the table's width.  Aim for several
-// waves of two resident CTAs per SM over the widest possible rows, with
-// splits of at most 32 pages (512 KiB of K+V per kv head).
-static int auto_chunk(const pkv_pool* pool, int tokens, int pages)
-{
-    const int64_t units = (int64_t)tokens * pool->cfg.kv_heads;
-    const int64_t total = units * pages;
-    const int64_t target = (int64_t)pool->num_sms * 2 * 6;
-    int64_t chunk = (total + target - 1) / target;
-    if (chunk < 1) chunk = 1;
-    if (chunk > 32) chunk = 32;
-    return (int)chunk;
-}
-
+// Workspace of one call: per token its attended length and table row (step
+// mode), the prefix of pages over tokens, a validity flag per (token, kv head)
+// unit, and one partial (4 heads x 128 fp32 + 4 log-sum-exps) per piece of a
+// unit split between CTAs: unit u's piece in CTA c sits at u + c, so U + C slots.
 Plan make_plan(const pkv_pool* pool, int tokens, int pages)
 {
     Plan pl;
     pl.tokens = tokens;
     pl.pages = pages;
-    pl.chunk = pool->split_pages > 0 ? pool->split_pages : auto_chunk(pool, tokens, pages);
-    if (pl.chunk > pages) pl.chunk = pages;
-    pl.max_splits = (pages + pl.chunk - 1) / pl.chunk;
-    const size_t H = (size_t)pool->cfg.heads, D = (size_t)pool->cfg.head_dim;
+    pl.ctas = pool->ctas_override > 0 ? pool->ctas_override : pool->ctas_per_sm * pool->num_sms;
+    const size_t G = (size_t)pool->cfg.kv_heads;
+    const size_t units = (size_t)tokens * G;
+    const size_t slots = units + (size_t)pl.ctas;
     size_t off = 0;
     pl.off_len = off;
     off = align_up(off + sizeof(int32_t) * tokens, 256);
     pl.off_row = off;
     off = align_up(off + sizeof(int32_t) * tokens, 256);
-    pl.off_qhat = off;
-    off = align_up(off + sizeof(float) * tokens * H * D, 256);
-    if (pl.max_splits > 1) {
-        pl.off_po = off;
-        off = align_up(off + sizeof(float) * tokens * H * pl.max_splits * D, 256);
-        pl.off_plse = off;
-        off = align_up(off + sizeof(float) * tokens * H * pl.max_splits, 256);
-    } else {
-        pl.off_po = pl.off_plse = 0;
-    }
+    pl.off_prefix = off;
+    off = align_up(off + sizeof(int32_t) * (tokens + 1), 256);
+    pl.off_unit_ok = off;
+    off = align_up(off + sizeof(int32_t) * units, 256);
+    pl.off_po = off;
+    off = align_up(off + sizeof(float) * slots * kGroup * kHeadDim, 256);
+    pl.off_plse = off;
+    off = align_up(off + sizeof(float) * slots * kGroup, 256);
     pl.total = off;
     return pl;
+}
+
+int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
+{
+    const bool decode = a.P == 0;
+    if (!decode && launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+    const bool timed = pool->timer_on;
+    const int slot = (int)(pool->timer_count % kTimerSlots);
+    if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
+    // programmatic dependent launch: the kernel is scheduled while the one
+    // before it drains, and waits for it before touching memory
+    if (launch_attn(pool, a, plan, decode, !timed, s) != cudaSuccess) return PKV_ECUDA;
+    if (timed) {
+        if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
+        pool->timer_count++;
+    }
+    if (launch_combine(pool, a, plan, decode, s) != cudaSuccess) return PKV_ECUDA;
+    return PKV_OK;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -106,22 +111,26 @@ static int check_config(const pkv_config* c)
     return PKV_OK;
 }
 
-// RoPE table: (cos, sin) of pos * theta^(-2i/head_dim), i < head_dim/2, for
-// every position < max_seq, in double precision (qwen3-8b Nest files,
+// RoPE tables: (cos, sin) of pos * theta^(-2i/head_dim), i < head_dim/2, for
+// every position < max_seq, computed in double (qwen3-8b Nest files,
 // src/rope.linnet tables; the pages evaluate the angle in f32, which at
-// position 40959 is off by up to ~2e-3 rad).  The k rotation uses it in
-// double so the written K is within one rounding of the exact value even when
-// the two rotated terms cancel; q uses it rounded to fp32.
-static void rope_table(const pkv_config& c, std::vector<double2>& cs)
+// position 40959 is off by up to ~2e-3 rad) and kept as two fp32 tables: hi,
+// the nearest fp32 values (q uses these), and lo, the remainders (k uses
+// hi + lo, so its rotation keeps the double table's accuracy).
+static void rope_tables(const pkv_config& c, std::vector<float2>& hi, std::vector<float2>& lo)
 {
     const int half = c.head_dim / 2;
-    cs.resize((size_t)c.max_seq * half);
+    hi.resize((size_t)c.max_seq * half);
+    lo.resize((size_t)c.max_seq * half);
     std::vector<double> inv(half);
     for (int i = 0; i < half; ++i) inv[i] = std::pow(c.rope_theta, -2.0 * i / (double)c.head_dim);
     for (int p = 0; p < c.max_seq; ++p)
         for (int i = 0; i < half; ++i) {
             const double a = (double)p * inv[i];
-            cs[(size_t)p * half + i] = make_double2(std::cos(a), std::sin(a));
+            const double cs = std::cos(a), sn = std::sin(a);
+            const float ch = (float)cs, sh = (float)sn;
+            hi[(size_t)p * half + i] = make_float2(ch, sh);
+            lo[(size_t)p * half + i] = make_float2((float)(cs - (double)ch), (float)(sn - (double)sh));
         }
 }
 
@@ -151,7 +160,7 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
     p->num_slots = num_slots;
     p->owns_kv = owns;
     const size_t kv_bytes = (size_t)cfg->kv_heads * num_slots * cfg->head_dim * 2;
-    const size_t tab = (size_t)cfg->max_seq * (cfg->head_dim / 2) * sizeof(double2);
+    const size_t tab = (size_t)cfg->max_seq * (cfg->head_dim / 2) * sizeof(float2);
     bool fail = false;
     if (owns) {
         fail |= cudaMalloc(&p->k, kv_bytes) != cudaSuccess;
@@ -160,26 +169,30 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
         p->k = k;
         p->v = v;
     }
-    fail |= !fail && cudaMalloc(reinterpret_cast<void**>(&p->rope), tab) != cudaSuccess;
+    fail |= !fail && cudaMalloc(reinterpret_cast<void**>(&p->rope_hi), tab) != cudaSuccess;
+    fail |= !fail && cudaMalloc(reinterpret_cast<void**>(&p->rope_lo), tab) != cudaSuccess;
     fail |= !fail && cudaMalloc(reinterpret_cast<void**>(&p->err), 256) != cudaSuccess;
     if (fail) {
         cudaGetLastError();
         pkv_pool_free(p);
         return PKV_ENOMEM;
     }
-    std::vector<double2> cs;
-    rope_table(*cfg, cs);
+    std::vector<float2> rhi, rlo;
+    rope_tables(*cfg, rhi, rlo);
     bool ok = true;
     if (owns) {
         ok &= cudaMemsetAsync(p->k, 0, kv_bytes, s) == cudaSuccess;
         ok &= cudaMemsetAsync(p->v, 0, kv_bytes, s) == cudaSuccess;
     }
-    ok &= cudaMemcpyAsync(p->rope, cs.data(), tab, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    ok &= cudaMemcpyAsync(p->rope_hi, rhi.data(), tab, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    ok &= cudaMemcpyAsync(p->rope_lo, rlo.data(), tab, cudaMemcpyHostToDevice, s) == cudaSuccess;
     ok &= cudaMemsetAsync(p->err, 0, 256, s) == cudaSuccess;
     ok &= cudaStreamSynchronize(s) == cudaSuccess;  // the host vectors die with this call
     ok &= make_tmap(&p->tmap_k, p->k, num_slots, cfg->kv_heads);
     ok &= make_tmap(&p->tmap_v, p->v, num_slots, cfg->kv_heads);
     ok &= configure_kernels() == cudaSuccess;
+    p->ctas_per_sm = attn_ctas_per_sm();
+    ok &= p->ctas_per_sm > 0;
     if (!ok) {
         cudaGetLastError();
         pkv_pool_free(p);
@@ -191,29 +204,13 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
 
 static bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-static int run_step(pkv_pool* pool, const StepArgs& a0, size_t ws_bytes, void* stream)
+static int run_step(pkv_pool* pool, const StepArgs& a, size_t ws_bytes, void* stream)
 {
-    StepArgs a = a0;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
-    const int tokens = a.P + a.rows;
-    Plan plan = make_plan(pool, tokens, a.pages);
+    const Plan plan = make_plan(pool, a.P + a.rows, a.pages);
     if (!a.ws || ws_bytes < plan.total) return PKV_EWORKSPACE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_prep(pool, a, plan, s);
-    if (e != cudaSuccess) return PKV_ECUDA;
-    const bool timed = pool->timer_on;
-    const int slot = (int)(pool->timer_count % kTimerSlots);
-    if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
-    e = launch_attn_decode(pool, a, plan, s);
-    if (e != cudaSuccess) return PKV_ECUDA;
-    if (timed) {
-        if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
-        pool->timer_count++;
-    }
-    e = launch_combine(pool, a, plan, s);
-    if (e != cudaSuccess) return PKV_ECUDA;
-    return PKV_OK;
+    return enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace pkv
@@ -272,7 +269,8 @@ int pkv_pool_free(pkv_pool* p)
         if (p->k) cudaFree(p->k);
         if (p->v) cudaFree(p->v);
     }
-    if (p->rope) cudaFree(p->rope);
+    if (p->rope_hi) cudaFree(p->rope_hi);
+    if (p->rope_lo) cudaFree(p->rope_lo);
     if (p->err) cudaFree(p->err);
     if (p->ev_start) {
         for (int i = 0; i < kTimerSlots; ++i) {
@@ -300,7 +298,7 @@ int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_t
 {
     if (!pool || !bytes || rows < 0 || prefill_tokens < 0 || rows + prefill_tokens <= 0 || pages <= 0)
         return PKV_EINVAL;
-    if ((int64_t)rows + prefill_tokens > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if ((int64_t)rows + prefill_tokens > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
     *bytes = make_plan(pool, rows + prefill_tokens, pages).total;
     return PKV_OK;
 }
@@ -311,8 +309,8 @@ int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, cons
 {
     if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !table || !out) return PKV_EINVAL;
     if (rows <= 0 || pages <= 0) return PKV_EINVAL;
-    if (rows > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
-    if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
+    if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
         !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(table, 4))
         return PKV_EINVAL;
     if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
@@ -330,8 +328,8 @@ int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const 
         !out)
         return PKV_EINVAL;
     if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
-    if ((int64_t)P + rows > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
-    if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
+    if ((int64_t)P + rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
         !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(prow, 4) || !aligned(step_positions, 4) ||
         !aligned(table, 4) || (slots && !aligned(slots, 4)))
         return PKV_EINVAL;
@@ -353,10 +351,10 @@ int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags)
     return PKV_OK;
 }
 
-int pkv_set_split_pages(pkv_pool* pool, int pages_per_split)
+int pkv_set_ctas(pkv_pool* pool, int ctas)
 {
-    if (!pool || pages_per_split < 0) return PKV_EINVAL;
-    pool->split_pages = pages_per_split;
+    if (!pool || ctas < 0) return PKV_EINVAL;
+    pool->ctas_override = ctas;
     return PKV_OK;
 }
 

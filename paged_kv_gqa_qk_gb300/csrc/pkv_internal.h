@@ -31,11 +31,13 @@ struct pkv_pool {
     bool owns_kv;
     void* k;               // bf16 [kv_heads][num_slots][head_dim]
     void* v;
-    double2* rope;         // (cos, sin) [max_seq][head_dim/2], double precision
+    float2* rope_hi;       // (cos, sin) [max_seq][head_dim/2]: fp32 nearest to the double values
+    float2* rope_lo;       // the double values minus rope_hi, in fp32
     uint32_t* err;         // sticky device error word
     CUtensorMap tmap_k;    // 3-D tiled view of K: {head_dim, num_slots, kv_heads}, box {64, 64, 1}, 128B swizzle
     CUtensorMap tmap_v;
-    int split_pages;       // 0 = automatic
+    int ctas_per_sm;       // resident attention CTAs per SM (occupancy)
+    int ctas_override;     // attention grid size; 0 = one wave (ctas_per_sm x SMs)
     // kernel timer
     bool timer_on;
     int64_t timer_count;
@@ -49,9 +51,8 @@ namespace pkv {
 struct Plan {
     int tokens;         // P + rows
     int pages;          // table width
-    int chunk;          // pages per split
-    int max_splits;     // ceil(pages / chunk)
-    size_t off_len, off_row, off_qhat, off_po, off_plse, total;
+    int ctas;           // attention grid size C
+    size_t off_len, off_row, off_prefix, off_unit_ok, off_po, off_plse, total;
 };
 
 Plan make_plan(const pkv_pool* pool, int tokens, int pages);
@@ -78,10 +79,19 @@ struct StepArgs {
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.
 cudaError_t configure_kernels();
+// Resident attention CTAs per SM (0 on error).
+int attn_ctas_per_sm();
 
 // Kernel launchers (pkv_kernels.cu).  Each returns a cudaError_t from the launch.
+//   decode: attn (decode mode, fuses validation + append) -> combine
+//   step:   prep (validation + append of every token) -> attn (step mode) -> combine
 cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
-cudaError_t launch_attn_decode(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
-cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
+cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& plan, bool decode_mode, bool pdl,
+                        cudaStream_t s);
+cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& plan, bool decode_mode,
+                           cudaStream_t s);
+
+// Enqueue one decode (a.P == 0) or step call on workspace a.ws; host checks done.
+int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
 
 }  // namespace pkv

@@ -1,13 +1,20 @@
 // Kernels of the paged-KV decode step (sm_103a).
 //
-//   prep_kernel        QK-norm + RoPE of q and k, page-slot append of k and v
-//                      (one CTA per token).
-//   attn_decode_kernel split-KV ("flash-decoding") attention over a token's
-//                      pages: one CTA per (token, kv head, page range); TMA
-//                      copies whole 16 KiB pages of K and V into a shared-
-//                      memory ring, four consumer warps run QK^T and PV on
-//                      mma.sync tensor cores with an online softmax.
-//   combine_kernel     log-sum-exp merge of the page ranges of a token.
+//   attn_kernel     persistent split-KV attention.  The work is the sequence
+//                   of (token, kv head, page) triples; each CTA streams an
+//                   equal slice of it, whatever the mix of row lengths.  A
+//                   producer warp streams the pages
+//                   through a shared-memory ring with TMA; four consumer warps
+//                   run QK^T and PV on mma.sync tensor cores with an online
+//                   softmax.  In decode mode the kernel also does the per-token
+//                   work before attention: it validates each row, norms and
+//                   ropes the query heads it attends with, and appends the
+//                   row's new k and v (see attn_kernel).
+//   combine_kernel  log-sum-exp merge of the pieces of a (token, kv head) that
+//                   several CTAs shared; zero outputs for skipped tokens.
+//   prep_kernel     step mode only: validates every token and appends all k/v
+//                   before any attention (the prompt tokens of a chunk read
+//                   each other's keys).
 //
 // Source of the computation: qwen3-8b Nest files, src/attention.linnet,
 // GroupedQueryAttention.decode_paged / step_paged (q_norm/k_norm -> rope_rows
@@ -23,48 +30,12 @@ namespace pkv {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
-// =====================================================================================
-// G1: QK-norm + RoPE + KV append
-// =====================================================================================
-struct PrepParams {
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* k;
-    const __nv_bfloat16* v;
-    const __nv_bfloat16* qw;
-    const __nv_bfloat16* kw;
-    const int32_t* positions;       // [P]
-    const int32_t* prow;            // [P]
-    const int32_t* slots;           // [P] or null
-    const int32_t* step_positions;  // [rows]
-    const int32_t* table;           // [rows][pages]
-    int P, rows, pages, num_pages, max_seq, heads, kv_heads;
-    int64_t num_slots;
-    float eps;
-    const double2* rope;            // (cos, sin) [max_seq][64]
-    __nv_bfloat16* K;               // [kv_heads][num_slots][128]
-    __nv_bfloat16* V;
-    float* qhat;                    // [tokens][heads][128]  normed + roped q
-    int32_t* tok_len;               // [tokens]  attended length, 0 = skip
-    int32_t* tok_row;               // [tokens]  table row
-    uint32_t* err;
-};
-
 __device__ __forceinline__ void unpack4(uint2 r, float (&x)[4])
 {
     x[0] = __uint_as_float(r.x << 16);
     x[1] = __uint_as_float(r.x & 0xffff0000u);
     x[2] = __uint_as_float(r.y << 16);
     x[3] = __uint_as_float(r.y & 0xffff0000u);
-}
-
-// Round a double to bf16, nearest-even, with one rounding: truncate to fp32
-// and mark inexactness in the last bit (round-to-odd; fp32 keeps 16 more bits
-// than bf16), then round that to bf16.
-__device__ __forceinline__ __nv_bfloat16 double_to_bf16_rn(double x)
-{
-    float f = __double2float_rz(x);
-    if ((double)f != x) f = __uint_as_float(__float_as_uint(f) | 1u);
-    return __float2bfloat16_rn(f);
 }
 
 __device__ __forceinline__ uint2 pack4(const float (&y)[4])
@@ -75,9 +46,78 @@ __device__ __forceinline__ uint2 pack4(const float (&y)[4])
     return r;
 }
 
-// One CTA (4 warps) per token.  Lane l of a warp owns elements 4l..4l+3 of a
-// head vector; the rotate-half partner of element i < 64 is element i + 64,
-// held by lane l ^ 16.
+// k after QK-norm + rotate-half RoPE, for the warp that holds one k head
+// (lane l: elements 4l..4l+3; the rotate-half partner of element i < 64 is
+// i + 64, in lane l ^ 16):
+//   RMSNorm: x / sqrt(mean(x^2) + eps) * w;  RoPE: y*cos + rotate_half(y)*sin.
+// Both are linear in y, so the normaliser goes last:
+//   r = inv * a,  a = u*cos -/+ u'*sin,  u = x*w (exact in fp32: bf16 x bf16).
+// k is stored in bf16, and when the two terms of a cancel, plain fp32 loses
+// far more than a bf16 ulp.  So a is formed without error growth: cos and sin
+// come as fp32 hi + lo pairs of the double values, the products' rounding
+// errors are recovered exactly with fma and the sum's with two-sum; the
+// result has fp32 accuracy relative to a itself, and rounds to within one
+// bf16 ulp of the exact value.
+__device__ __forceinline__ float rotate_exact(float u, float up, float2 hi, float2 lo)
+{
+    const float p1 = __fmul_rn(u, hi.x), e1 = __fmaf_rn(u, hi.x, -p1);
+    const float p2 = __fmul_rn(up, hi.y), e2 = __fmaf_rn(up, hi.y, -p2);
+    const float s = __fadd_rn(p1, p2);
+    const float bp = __fsub_rn(s, p1);
+    const float e3 = __fadd_rn(__fsub_rn(p1, __fsub_rn(s, bp)), __fsub_rn(p2, bp));
+    const float lo_terms = __fmaf_rn(u, lo.x, __fmaf_rn(up, lo.y, __fadd_rn(__fadd_rn(e1, e2), e3)));
+    return __fadd_rn(s, lo_terms);
+}
+
+// The warp's normed + roped k as 4 bf16 (this lane's elements).
+//   kraw: this lane's 4 raw bf16;  wk: its k_norm weights;
+//   rhi/rlo: (cos, sin) hi and lo parts of the token's position, [64].
+__device__ __forceinline__ uint2 norm_rope_k(uint2 kraw, const float (&wk)[4], const float2* rhi, const float2* rlo,
+                                             float eps, int lane)
+{
+    float x[4];
+    unpack4(kraw, x);
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    const float inv = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+    const float sgn = lane < 16 ? -1.f : 1.f;
+    __nv_bfloat16 r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int f = 4 * (lane & 15) + i;
+        const float u = x[i] * wk[i];
+        const float partner = sgn * __shfl_xor_sync(kFull, u, 16);
+        r[i] = __float2bfloat16_rn(__fmul_rn(rotate_exact(u, partner, rhi[f], rlo[f]), inv));
+    }
+    return make_uint2(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]));
+}
+
+// =====================================================================================
+// prep_kernel (step mode): validate every token, append every token's k and v
+// =====================================================================================
+struct PrepParams {
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* kw;
+    const int32_t* positions;       // [P]
+    const int32_t* prow;            // [P]
+    const int32_t* slots;           // [P] or null
+    const int32_t* step_positions;  // [rows]
+    const int32_t* table;           // [rows][pages]
+    int P, rows, pages, num_pages, max_seq, kv_heads;
+    int64_t num_slots;
+    float eps;
+    const float2* rope_hi;          // (cos, sin) [max_seq][64], fp32 nearest to the double values
+    const float2* rope_lo;          // the double values minus rope_hi, in fp32
+    __nv_bfloat16* K;               // [kv_heads][num_slots][128]
+    __nv_bfloat16* V;
+    int32_t* tok_len;               // [tokens]  attended length, 0 = skip
+    int32_t* tok_row;               // [tokens]  table row
+    uint32_t* err;
+};
+
+// One CTA (4 warps) per token; warp w appends kv heads w, w+4, ...
 __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
 {
     const int t = blockIdx.x;
@@ -121,92 +161,33 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
             slot = (int64_t)trow[pos / kPageSize] * kPageSize + pos % kPageSize;
         }
     }
-    if (!active || e) {
-        if (tid == 0) {
-            p.tok_len[t] = 0;
-            p.tok_row[t] = 0;
-            if (e) atomicOr(p.err, e);
-        }
-        return;
-    }
     if (tid == 0) {
-        p.tok_len[t] = pos + 1;
-        p.tok_row[t] = row;
+        const bool ok = active && !e;
+        p.tok_len[t] = ok ? pos + 1 : 0;
+        p.tok_row[t] = ok ? row : 0;
+        if (e) atomicOr(p.err, e);
     }
+    if (!active || e) return;
 
-    const int H = p.heads, G = p.kv_heads;
-    const int fi = 4 * (lane & 15);  // frequency index of this lane's first element
-    double cosd[4], sind[4];
-    float cosv[4], sinv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const double2 cs = p.rope[(int64_t)pos * kRopeHalf + fi + i];
-        cosd[i] = cs.x;
-        sind[i] = cs.y;
-        cosv[i] = (float)cs.x;
-        sinv[i] = (float)cs.y;
-    }
-    float wq[4], wk[4];
-    unpack4(*reinterpret_cast<const uint2*>(p.qw + 4 * lane), wq);
+    float wk[4];
     unpack4(*reinterpret_cast<const uint2*>(p.kw + 4 * lane), wk);
-    const float sgn = lane < 16 ? -1.f : 1.f;
-
-    for (int task = warp; task < H + 2 * G; task += 4) {
-        if (task < H + G) {
-            const bool isq = task < H;
-            const __nv_bfloat16* src = isq ? p.q + ((int64_t)t * H + task) * kHeadDim
-                                           : p.k + ((int64_t)t * G + (task - H)) * kHeadDim;
-            float x[4];
-            unpack4(*reinterpret_cast<const uint2*>(src + 4 * lane), x);
-            float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-            // RMSNorm over the head's 128 elements: x / sqrt(mean(x^2) + eps) * w,
-            // then rotate-half RoPE: y*cos + rotate_half(y)*sin, rotate_half = (-y2, y1).
-            // Both are linear in y, so the normaliser is applied last:
-            //   r = inv * (u*cos -/+ u'*sin),  u = x*w  (exact in fp32: bf16 x bf16).
-            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-            float u[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) u[i] = x[i] * (isq ? wq[i] : wk[i]);
-            if (isq) {
-                float r[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float partner = __shfl_xor_sync(kFull, u[i], 16);
-                    r[i] = inv * (u[i] * cosv[i] + sgn * partner * sinv[i]);
-                }
-                *reinterpret_cast<float4*>(p.qhat + ((int64_t)t * H + task) * kHeadDim + 4 * lane) =
-                    make_float4(r[0], r[1], r[2], r[3]);
-            } else {
-                // k is stored in bf16: rotate in double so cancellation between the
-                // two terms cannot cost more than the final rounding
-                __nv_bfloat16 r[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float partner = __shfl_xor_sync(kFull, u[i], 16);
-                    const double a = fma((double)(sgn * partner), sind[i], (double)u[i] * cosd[i]);
-                    r[i] = double_to_bf16_rn(a * (double)inv);
-                }
-                const int g = task - H;
-                *reinterpret_cast<uint2*>(p.K + ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane) =
-                    make_uint2(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]));
-            }
-        } else {
-            const int g = task - H - G;  // v is written as given
-            const uint2 raw = *reinterpret_cast<const uint2*>(p.v + ((int64_t)t * G + g) * kHeadDim + 4 * lane);
-            *reinterpret_cast<uint2*>(p.V + ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane) = raw;
-        }
+    const float2* rhi = p.rope_hi + (int64_t)pos * kRopeHalf;
+    const float2* rlo = p.rope_lo + (int64_t)pos * kRopeHalf;
+    for (int g = warp; g < p.kv_heads; g += 4) {
+        const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim;
+        const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim;
+        const uint2 kraw = *reinterpret_cast<const uint2*>(p.k + src + 4 * lane);
+        const uint2 vraw = *reinterpret_cast<const uint2*>(p.v + src + 4 * lane);
+        *reinterpret_cast<uint2*>(p.K + dst + 4 * lane) = norm_rope_k(kraw, wk, rhi, rlo, p.eps, lane);
+        *reinterpret_cast<uint2*>(p.V + dst + 4 * lane) = vraw;  // v is written as given
     }
 }
 
 cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
 {
     PrepParams p;
-    p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.k = static_cast<const __nv_bfloat16*>(a.k);
     p.v = static_cast<const __nv_bfloat16*>(a.v);
-    p.qw = static_cast<const __nv_bfloat16*>(a.q_norm_w);
     p.kw = static_cast<const __nv_bfloat16*>(a.k_norm_w);
     p.positions = a.positions;
     p.prow = a.prow;
@@ -218,14 +199,13 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.pages = a.pages;
     p.num_pages = pool->num_pages;
     p.max_seq = pool->cfg.max_seq;
-    p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.num_slots = pool->num_slots;
     p.eps = static_cast<float>(pool->cfg.eps);
-    p.rope = pool->rope;
+    p.rope_hi = pool->rope_hi;
+    p.rope_lo = pool->rope_lo;
     p.K = static_cast<__nv_bfloat16*>(pool->k);
     p.V = static_cast<__nv_bfloat16*>(pool->v);
-    p.qhat = reinterpret_cast<float*>(a.ws + plan.off_qhat);
     p.tok_len = reinterpret_cast<int32_t*>(a.ws + plan.off_len);
     p.tok_row = reinterpret_cast<int32_t*>(a.ws + plan.off_row);
     p.err = pool->err;
@@ -234,58 +214,169 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
 }
 
 // =====================================================================================
-// G2: split-KV decode attention
+// attn_kernel: persistent split-KV attention with a static + dynamic work split
 // =====================================================================================
 //
-// CTA (token t, kv head g, split s) attends the 4 query heads of kv head g
-// over pages [s*chunk, min(npages, (s+1)*chunk)) of the token's row.
+// Work order.  Tokens in order; within a token its kv heads; within a kv head
+// its pages 0..npg-1: unit u = t*G + g covers global pages
+// [G*pre[t] + g*npg[t], + npg[t]) with pre the exclusive prefix of npg over
+// tokens, T = G*sum(npg) pages in all.  CTA c of C' = min(C, T) streams the
+// slice [c*T/C', (c+1)*T/C'); CTAs beyond C' idle.  The piece of a unit inside
+// one slice is a segment.  A unit wholly inside one slice is written out
+// directly; otherwise each piece leaves a partial (O/l and the base-2
+// log-sum-exp, for the 4 query heads) at index u + c -- unique, because units
+// and slices both increase along the sequence -- and combine_kernel merges them.
 //
-// Warp roles: warps 0-3 consume, warp 4 produces.  The producer streams the
-// pages through a ring of kStages stages; each stage is one page of K and one
-// of V for kv head g, each copied as two 64x64 boxes (head-dim halves) with
-// 128-byte swizzle, so ldmatrix reads them without bank conflicts.
-//
-// Consumer warp w takes positions 16w..16w+15 of every page.
-//   QK^T:  S[16 pos][8 cols] = K_tile[16 pos][128] * Qb[128][8 cols]
+// Per page, consumer warp w takes positions 16w..16w+15:
+//   QK^T:  S[16 pos][8 cols] = K_tile[16][128] * Qb[128][8]
 //          cols 0-3 = bf16 head of q (heads 4g..4g+3, scaled by log2(e)/sqrt(128)),
-//          cols 4-7 = bf16 of the remainder: S = col h + col h+4 carries q to
-//          ~16 bits, so the logits keep fp32-level accuracy.
-//   PV:    O^T[128 dims][8 cols] += V_tile^T[128][16 pos] * Pb[16 pos][8 cols]
+//          cols 4-7 = bf16 of the remainder; S = col h + col h+4 keeps ~16 bits of q.
+//   PV:    O^T[128][8] += V_tile^T[128][16 pos] * Pb[16 pos][8]
 //          cols 0-3 = bf16(p), cols 4-7 = bf16(p - bf16(p)); O = col h + col h+4.
-// The softmax is kept per warp (running max m and sum l per head, base 2);
-// the four warps' (m, l, O) are merged through shared memory at the end.
+// Softmax state (running max m, sum l, per head, base 2) is per warp; the four
+// warps are merged through shared memory, in a fixed order, at the end of
+// each segment.
+//
+// Decode mode appends each row's new k and v: the CTA holding a unit's last
+// page receives the row's raw k/v with the segment, and the consumer warp
+// that owns the new slot's position norms and ropes k, writes it and v into
+// its staged copy of the page and to the pool.  Each (row, kv head) slot is
+// read only by that row (a documented condition of pkv_decode), so no other
+// CTA waits for the write.
 struct AttnParams {
-    const float* qhat;       // [tokens][heads][128]
-    const int32_t* tok_len;  // [tokens]
-    const int32_t* tok_row;  // [tokens]
-    const int32_t* table;    // [rows][pages]
-    int pages, chunk, max_splits, heads, kv_heads;
-    __nv_bfloat16* out;      // [tokens][heads][128]
-    float* part_o;           // [tokens][heads][max_splits][128]
-    float* part_lse;         // [tokens][heads][max_splits]   (base-2 log-sum-exp)
+    const __nv_bfloat16* q;   // [ntok][heads][128] projected q (normed + roped here)
+    const __nv_bfloat16* k;   // [ntok][kv_heads][128]  (decode mode: appended here)
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* qw;
+    const __nv_bfloat16* kw;
+    const int32_t* positions; // decode mode: [ntok], token t is table row t
+    const int32_t* tok_len;   // step mode: [ntok] from prep_kernel, 0 = skip
+    const int32_t* tok_row;   // step mode: [ntok]
+    const int32_t* table;     // [rows][pages]
+    const float2* rope_hi;    // (cos, sin) [max_seq][64], fp32 nearest to the double values
+    const float2* rope_lo;    // the double values minus rope_hi, in fp32 (k only)
+    __nv_bfloat16* K;         // pool
+    __nv_bfloat16* V;
+    __nv_bfloat16* out;       // [ntok][heads][128]
+    float* part_o;            // [U + C][4][128]
+    float* part_lse;          // [U + C][4]
+    int32_t* prefix;          // [ntok + 1], written by CTA 0 for combine_kernel
+    int32_t* unit_ok;         // [U], written by the CTA holding each unit's first page
     uint32_t* err;
+    int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode;
+    int64_t num_slots;
+    float eps;
 };
 
 constexpr int kConsumerWarps = 4;
+constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageBytes = 4 * 8192;  // K lo, K hi, V lo, V hi
+// Per stage, for a segment's first page: raw q of the 4 heads (1 KiB) and the
+// (cos, sin) hi parts of the token's position (512 B); when the segment holds
+// the row's new slot (decode mode) also the lo parts (512 B) and the raw k
+// and v (256 B each).
+constexpr int kSideBytes = 2560;
+constexpr int kSideQ = 0, kSideRopeHi = 1024, kSideRopeLo = 1536, kSideK = 2048, kSideV = 2304;
+
+constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagValid = 4, kFlagComplete = 8, kFlagHasLast = 16,
+              kFlagAppend = 32;
 
 template <int kStages>
 struct AttnSmem {
-    static constexpr int kRing = kStages * kStageBytes;
-    static constexpr int kMergeO = kRing;                                   // float [4 warps][4 heads][128]
-    static constexpr int kMergeM = kMergeO + kConsumerWarps * 4 * 128 * 4;  // float [4][4]
-    static constexpr int kMergeL = kMergeM + 64;                            // float [4][4]
-    static constexpr int kBars = kMergeL + 64;                              // uint64 full[kStages], empty[kStages]
-    static constexpr int kFlag = kBars + 2 * 8 * kStages;
+    static constexpr int kSide = kStages * kStageBytes;
+    static constexpr int kM = kSide + kStages * kSideBytes;  // float [4 warps][4 heads]
+    static constexpr int kL = kM + 64;                        // float [4][4]
+    static constexpr int kMeta = kL + 64;                     // int4 [stages][2]
+    static constexpr int kScan = kMeta + kStages * 32;        // int [8]
+    static constexpr int kSum = kScan + 32;                   // int [threads] first token, int [threads] prefix
+    static constexpr int kW = kSum + 2 * kAttnThreads * 4;    // bf16 q_norm_w [128], k_norm_w [128]
+    static constexpr int kBars = kW + 512;                    // u64 full[S], empty[S], group
+    static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);
     static constexpr int kBytes = kFlag + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
 };
 
+__device__ __forceinline__ int npg_of(const AttnParams& p, int t)
+{
+    if (p.decode_mode) {
+        const int pos = p.positions[t];
+        return (pos >= 0 && pos < p.max_seq && pos < p.pages * kPageSize) ? pos / kPageSize + 1 : 0;
+    }
+    const int len = p.tok_len[t];
+    return len > 0 ? (len + kPageSize - 1) / kPageSize : 0;
+}
+
+__device__ __forceinline__ void token_info(const AttnParams& p, int t, int& row, int& len)
+{
+    if (p.decode_mode) {
+        row = t;
+        len = p.positions[t] + 1;
+    } else {
+        row = p.tok_row[t];
+        len = p.tok_len[t];
+    }
+}
+
+// The four consumer warps meet at an mbarrier (bounded wait, unlike bar.sync).
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int lane)
+{
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait_spin(bar, phase & 1);
+    ++phase;
+    return ok;
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Warp-wide: the token t holding global page x (x < T) and its prefix pre[t],
+// from the per-thread summaries of the prologue (first token and prefix of each
+// thread's run of tokens) and one pass over that run.
+__device__ __forceinline__ void find_token(const AttnParams& p, const int* sT0, const int* sP0, int64_t x, int lane,
+                                           int& t_out, int& pre_out)
+{
+    const int G = p.kv_heads;
+    int lo = 0, hi = kAttnThreads - 1;
+    while (lo < hi) {  // last run whose prefix starts at or before x
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)G * sP0[mid] <= x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    int t = sT0[lo], pre = sP0[lo];
+    for (;;) {
+        const int tt = t + lane;
+        const int n = tt < p.ntok ? npg_of(p, tt) : 0;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int before = pre + incl - n;
+        const bool hit = n > 0 && (int64_t)G * before <= x && x < (int64_t)G * (before + n);
+        const unsigned m = __ballot_sync(kFull, hit);
+        if (m) {
+            const int l = __ffs(m) - 1;
+            t_out = __shfl_sync(kFull, tt, l);
+            pre_out = __shfl_sync(kFull, before, l);
+            return;
+        }
+        t += 32;
+        pre += __shfl_sync(kFull, incl, 31);
+    }
+}
+
 template <int kStages>
 __global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                       AttnParams p)
+    attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnParams p)
 {
     using L = AttnSmem<kStages>;
     extern __shared__ uint8_t smem_raw[];
@@ -294,137 +385,302 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     uint8_t* sbase = smem_raw + (base - raw_base);
     const uint32_t bar_full = base + L::kBars;
     const uint32_t bar_empty = bar_full + 8 * kStages;
+    const uint32_t bar_group = bar_empty + 8 * kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kFlag);
+    float* sM = reinterpret_cast<float*>(sbase + L::kM);
+    float* sL = reinterpret_cast<float*>(sbase + L::kL);
+    int4* sMeta = reinterpret_cast<int4*>(sbase + L::kMeta);
+    int* sScan = reinterpret_cast<int*>(sbase + L::kScan);
+    int* sT0 = reinterpret_cast<int*>(sbase + L::kSum);
+    int* sP0 = sT0 + kAttnThreads;
+    uint2* sW = reinterpret_cast<uint2*>(sbase + L::kW);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int lin = blockIdx.x;
-    const int s = lin % p.max_splits;
-    const int tg = lin / p.max_splits;
-    const int g = tg % p.kv_heads;
-    const int t = tg / p.kv_heads;
-    const int H = p.heads;
+    const int G = p.kv_heads, H = p.heads;
+    const int C = gridDim.x, c = blockIdx.x;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(bar_full + 8 * i, 1);
             mbar_init(bar_empty + 8 * i, kConsumerWarps);
         }
+        mbar_init(bar_group, kConsumerWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kConsumerWarps && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
+    // combine_kernel may be scheduled now: its CTAs wait for this grid to finish.
+    // (Every CTA of this grid is resident from the start, so they cannot block it.)
+    pdl_launch_dependents();
     __syncthreads();
-    pdl_wait();  // everything below reads what the prep kernel wrote
+    // Everything below reads the call's inputs and the pool, which the kernel
+    // before this one on the stream may have written.
+    pdl_wait();
 
-    const int len = p.tok_len[t];
-    if (len == 0) {  // skipped token: split 0 writes zeros for this kv head's query heads
-        if (s == 0) {
-            for (int i = tid; i < kGroup * kHeadDim / 4; i += kAttnThreads) {
-                const int h = i / (kHeadDim / 4), d = 4 * (i % (kHeadDim / 4));
-                *reinterpret_cast<uint2*>(p.out + ((int64_t)t * H + g * kGroup + h) * kHeadDim + d) =
-                    make_uint2(0u, 0u);
-            }
-        }
-        return;
+    // the norm weights, read once here (under the kernel's own streaming a
+    // global load can wait microseconds)
+    if (tid < 32) sW[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
+    else if (tid < 64) sW[tid] = reinterpret_cast<const uint2*>(p.kw)[tid - 32];
+
+    // ---- pages per token and their exclusive prefix over tokens (every CTA computes it)
+    const int nt = p.ntok;
+    const int per = (nt + kAttnThreads - 1) / kAttnThreads;
+    const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
+    int local = 0;
+    for (int t = t0; t < t1; ++t) local += npg_of(p, t);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
     }
-    const int npg = (len + kPageSize - 1) / kPageSize;
-    const int nsplit = (npg + p.chunk - 1) / p.chunk;
-    if (s >= nsplit) return;
-    const int pg0 = s * p.chunk;
-    const int n = min(npg, pg0 + p.chunk) - pg0;
-    const int row = p.tok_row[t];
+    if (lane == 31) sScan[warp] = incl;
+    __syncthreads();
+    int total = 0, warp_base = 0;
+#pragma unroll
+    for (int w = 0; w < kAttnThreads / 32; ++w) {
+        const int v = sScan[w];
+        warp_base += (w < warp) ? v : 0;
+        total += v;
+    }
+    const int excl = warp_base + incl - local;
+    sT0[tid] = t0;
+    sP0[tid] = excl;
+    if (c == 0) {
+        int run = excl;
+        for (int t = t0; t < t1; ++t) {
+            p.prefix[t] = run;
+            run += npg_of(p, t);
+        }
+        if (tid == kAttnThreads - 1) p.prefix[nt] = total;
+    }
+    __syncthreads();
+    const int64_t T = (int64_t)G * total;
+    const int Ce = (int)min((int64_t)C, T);  // never more slices than pages: none is empty
+    if (c >= Ce) return;
+    const int64_t gb = (int64_t)c * T / Ce, ge = (int64_t)(c + 1) * T / Ce;
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------------ producer
-        const int32_t* trow = p.table + (int64_t)row * p.pages + pg0;
-        const uint64_t pol = l2_policy_evict_first();
-        int issued = 0;
+    if (warp == kProducerWarp) {
+        // ================================================================ producer
+        int i = 0;  // ring items issued
         bool ok = true;
-        for (int b0 = 0; b0 < n && ok; b0 += 32) {
-            const int mine = (b0 + lane < n) ? trow[b0 + lane] : 0;
-            const int cnt = min(32, n - b0);
-            for (int j = 0; j < cnt; ++j) {
-                const int i = b0 + j;
-                const int page = __shfl_sync(kFull, mine, j);
-                const int st = i % kStages;
-                if (i >= kStages) {
-                    if (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag) {
-                        ok = false;
-                        break;
-                    }
+        const uint64_t pol = l2_policy_evict_first();
+        int t, pre;
+        find_token(p, sT0, sP0, gb, lane, t, pre);
+        int64_t St = (int64_t)G * pre;  // global index of (t, kv head 0, page 0)
+        int64_t x = gb;
+        while (x < ge && ok) {
+            const int n = npg_of(p, t);
+            const int64_t off = x - St;
+            const int g = (int)(off / n), j = (int)(off % n);
+            const int seg = (int)min((int64_t)(n - j), ge - x);
+            int row, len;
+            token_info(p, t, row, len);
+            const int pos = len - 1;
+            const int32_t* trow = p.table + (int64_t)row * p.pages;
+            bool valid = true;
+            if (p.decode_mode) {  // every page the row will read must be a pool page
+                int bad = 0;
+                for (int q = lane; q < n; q += 32) {
+                    const int id = trow[q];
+                    bad |= (id < 0 || id >= p.num_pages);
                 }
+                valid = !__any_sync(kFull, bad);
+            }
+            const int u = t * G + g;
+            if (j == 0 && lane == 0) {
+                p.unit_ok[u] = valid ? 1 : 0;
+                if (!valid && g == 0) atomicOr(p.err, PKV_DEVERR_PAGE);
+            }
+            const bool has_last = j + seg == n;
+            const bool append = p.decode_mode && valid && has_last;
+            const int seg_flags = (valid ? kFlagValid : 0) | ((j == 0 && has_last) ? kFlagComplete : 0);
+            for (int s = 0; s < seg; ++s, ++i) {
+                const int jj = j + s, st = i % kStages;
+                if (i >= kStages && (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                int page = 0;
+                if (lane == 0 && valid) page = trow[jj];
+                page = __shfl_sync(kFull, page, 0);
                 if (lane == 0) {
-                    const uint32_t dst = base + st * kStageBytes;
+                    const int flags = seg_flags | (s == 0 ? kFlagFirst : 0) | (s == seg - 1 ? kFlagLast : 0) |
+                                      ((s == 0 && append) ? kFlagHasLast : 0) |
+                                      ((append && jj == n - 1) ? kFlagAppend : 0);
+                    sMeta[2 * st] = make_int4(t, g, jj, len);
+                    sMeta[2 * st + 1] = make_int4(flags, u + c, page, 0);
                     const uint32_t fb = bar_full + 8 * st;
-                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    const uint32_t dst = base + st * kStageBytes;
+                    uint32_t bytes = kStageBytes;
+                    if (s == 0) bytes += 1536 + (append ? 1024 : 0);
+                    mbar_arrive_expect_tx(fb, bytes);
                     const int y = page * kPageSize;
                     tma_load_3d(dst, &tmK, 0, y, g, fb, pol);
                     tma_load_3d(dst + 8192, &tmK, 64, y, g, fb, pol);
                     tma_load_3d(dst + 16384, &tmV, 0, y, g, fb, pol);
                     tma_load_3d(dst + 24576, &tmV, 64, y, g, fb, pol);
+                    if (s == 0) {
+                        const uint32_t side = base + L::kSide + st * kSideBytes;
+                        bulk_copy(side + kSideQ, p.q + ((int64_t)t * H + g * kGroup) * kHeadDim, 1024, fb);
+                        bulk_copy(side + kSideRopeHi, p.rope_hi + (int64_t)pos * kRopeHalf, 512, fb);
+                        if (append) {
+                            const int64_t kv = ((int64_t)t * G + g) * kHeadDim;
+                            bulk_copy(side + kSideRopeLo, p.rope_lo + (int64_t)pos * kRopeHalf, 512, fb);
+                            bulk_copy(side + kSideK, p.k + kv, 256, fb);
+                            bulk_copy(side + kSideV, p.v + kv, 256, fb);
+                        }
+                    }
                 }
-                ++issued;
                 __syncwarp();
             }
-        }
-        if (!ok) {
-            if (lane == 0) {
-                atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-                *abort_flag = 1;
-                // wait (bounded) for the copies still in flight before the CTA exits
-                for (int i = max(0, issued - kStages); i < issued; ++i)
-                    mbar_wait(bar_full + 8 * (i % kStages), (i / kStages) & 1);
+            x += seg;
+            if (ok && x < ge && x >= St + (int64_t)G * n) {  // next token that has pages
+                St += (int64_t)G * n;
+                do {
+                    ++t;
+                } while (npg_of(p, t) == 0);
             }
+        }
+        if (!ok && lane == 0) {
+            atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            // wait (bounded) for the copies still in flight before the CTA exits
+            for (int k2 = max(0, i - kStages); k2 < i; ++k2)
+                mbar_wait(bar_full + 8 * (k2 % kStages), (k2 / kStages) & 1);
         }
         return;
     }
 
-    // ---------------------------------------------------------------------- consumers
+    // ==================================================================== consumers
     const int gid = lane >> 2, tig = lane & 3;
-    // B fragments of q: col n = gid -> head gid&3, part gid>>2 (0 head, 1 remainder)
-    uint32_t bq[8][2];
-    {
-        const int hh = gid & 3;
-        const bool rem = gid >= 4;
-        const float* qh = p.qhat + ((int64_t)t * H + g * kGroup + hh) * kHeadDim;
-        const float sc = 1.4426950408889634f * 0.088388347648318440f;  // log2(e) / sqrt(128)
+    // This lane's B fragments hold dims 16ks + 2tig + {0, 1, 8, 9} (ks = 0..7) of
+    // one query head: 32 dims, closed under the rotate-half pairing (d, d +- 64),
+    // and the four lanes tig = 0..3 of a head hold all 128 of its dims.
+    const uint32_t* sWq = reinterpret_cast<const uint32_t*>(sW);  // q_norm_w as bf16 pairs
+    uint32_t wq2[8][2];  // q_norm weights of those dims, bf16 pairs
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int d0 = 16 * ks + 2 * tig;
-            const float2 xa = *reinterpret_cast<const float2*>(qh + d0);
-            const float2 xb = *reinterpret_cast<const float2*>(qh + d0 + 8);
-            const float xs[4] = {xa.x * sc, xa.y * sc, xb.x * sc, xb.y * sc};
-            __nv_bfloat16 hd[4], tl[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) split_bf16(xs[i], hd[i], tl[i]);
-            bq[ks][0] = rem ? pack_bf16(tl[0], tl[1]) : pack_bf16(hd[0], hd[1]);
-            bq[ks][1] = rem ? pack_bf16(tl[2], tl[3]) : pack_bf16(hd[2], hd[3]);
-        }
+    for (int ks = 0; ks < 8; ++ks) {
+        const int d0 = 16 * ks + 2 * tig;
+        wq2[ks][0] = sWq[d0 >> 1];
+        wq2[ks][1] = sWq[(d0 + 8) >> 1];
     }
-
-    float o[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float mA = -CUDART_INF_F, mB = -CUDART_INF_F, lA = 0.f, lB = 0.f;
+    float wk[4];
+    unpack4(sW[32 + lane], wk);
+    const float qscale = 1.4426950408889634f * 0.088388347648318440f;  // log2(e) / sqrt(128)
     const bool rem_lane = tig >= 2;  // this lane's S/O columns are the remainder columns
-    // source lanes of the P fragment (see the PV comment above)
     const int hh = gid & 3, prt = gid >> 2;
-    const int srcA = 4 * (2 * tig) + (hh >> 1) + 2 * prt;
+    const int srcA = 4 * (2 * tig) + (hh >> 1) + 2 * prt;  // lanes holding P for the PV B fragment
     const int srcB = srcA + 4;
     const int r_ld = lane & 7, j_ld = lane >> 3;
+    uint32_t gphase = 0;
+
+    uint32_t bq[8][2];
+    float o[8][4];
+    float mA = -CUDART_INF_F, mB = -CUDART_INF_F, lA = 0.f, lB = 0.f;
+    uint2 knew = make_uint2(0u, 0u), vnew = make_uint2(0u, 0u);  // the row's new k (normed, roped) and v
     bool ok = true;
 
-    for (int i = 0; i < n; ++i) {
+    const int nitems = (int)(ge - gb);
+    for (int i = 0; i < nitems; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
             ok = false;
             break;
         }
+        const int4 m1 = sMeta[2 * st + 1];
+        const int flags = m1.x;
+        const int4 m0 = sMeta[2 * st];
+        const int t = m0.x, g = m0.y, jj = m0.z, len = m0.w, pidx = m1.y, page = m1.z;
         const uint32_t kb = base + st * kStageBytes;
         const uint32_t vb = kb + 16384;
+
+        if (flags & kFlagFirst) {
+            const uint8_t* side = sbase + L::kSide + st * kSideBytes;
+            const float2* rpf = reinterpret_cast<const float2*>(side + kSideRopeHi);
+            // q of head 4g+hh, the dims of this lane's B fragments: QK-norm + RoPE in
+            // fp32 from the raw q and (cos, sin) staged with this page, scaled by
+            // log2(e)/sqrt(128), then split into bf16 head (cols 0-3) and remainder (cols 4-7)
+            {
+                const uint8_t* qrow = side + hh * 256;
+                uint32_t xr[8][2];
+                float ss = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int d0 = 16 * ks + 2 * tig;
+                    xr[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 2 * d0);
+                    xr[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 2 * (d0 + 8));
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float a = __uint_as_float(xr[ks][e] << 16), b = __uint_as_float(xr[ks][e] & 0xffff0000u);
+                        ss += a * a + b * b;
+                    }
+                }
+                ss += __shfl_xor_sync(kFull, ss, 1);
+                ss += __shfl_xor_sync(kFull, ss, 2);
+                const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * qscale;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {  // dims d (ks) and their partners d + 64 (ks + 4)
+                    float ylo[4], yhi[4];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int d = 16 * ks + 2 * tig + 8 * e + b;  // < 64
+                            const uint32_t xl = xr[ks][e], xh = xr[ks + 4][e];
+                            const uint32_t wl = wq2[ks][e], wh = wq2[ks + 4][e];
+                            const float ul = __uint_as_float(b ? (xl & 0xffff0000u) : (xl << 16)) *
+                                             __uint_as_float(b ? (wl & 0xffff0000u) : (wl << 16));
+                            const float uh = __uint_as_float(b ? (xh & 0xffff0000u) : (xh << 16)) *
+                                             __uint_as_float(b ? (wh & 0xffff0000u) : (wh << 16));
+                            const float2 cs = rpf[d];
+                            const float cf = cs.x, sf = cs.y;
+                            ylo[2 * e + b] = inv * (ul * cf - uh * sf);  // y[d]      = u[d] cos - u[d+64] sin
+                            yhi[2 * e + b] = inv * (uh * cf + ul * sf);  // y[d + 64] = u[d+64] cos + u[d] sin
+                        }
+                    }
+                    __nv_bfloat16 hl[4], tl[4], hh2[4], th[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        split_bf16(ylo[k], hl[k], tl[k]);
+                        split_bf16(yhi[k], hh2[k], th[k]);
+                    }
+                    bq[ks][0] = prt ? pack_bf16(tl[0], tl[1]) : pack_bf16(hl[0], hl[1]);
+                    bq[ks][1] = prt ? pack_bf16(tl[2], tl[3]) : pack_bf16(hl[2], hl[3]);
+                    bq[ks + 4][0] = prt ? pack_bf16(th[0], th[1]) : pack_bf16(hh2[0], hh2[1]);
+                    bq[ks + 4][1] = prt ? pack_bf16(th[2], th[3]) : pack_bf16(hh2[2], hh2[3]);
+                }
+            }
+            // the warp that owns the new slot's position prepares the row's k and v
+            if ((flags & kFlagHasLast) && warp == ((len - 1) % kPageSize) / 16) {
+                knew = norm_rope_k(*reinterpret_cast<const uint2*>(side + kSideK + 8 * lane), wk, rpf,
+                                   reinterpret_cast<const float2*>(side + kSideRopeLo), p.eps, lane);
+                vnew = *reinterpret_cast<const uint2*>(side + kSideV + 8 * lane);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            mA = mB = -CUDART_INF_F;
+            lA = lB = 0.f;
+        }
+
+        if ((flags & kFlagAppend) && warp == ((len - 1) % kPageSize) / 16) {
+            // the page holding the row's new slot: write k and v into the staged
+            // page (row r of the 128-byte-swizzled halves) and into the pool
+            const int r = (len - 1) % kPageSize;
+            const int half = lane >> 4, chunk = (lane & 15) >> 1;
+            const uint32_t off = half * 8192 + r * 128 + ((chunk ^ (r & 7)) << 4) + (lane & 1) * 8;
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + off), "r"(knew.x), "r"(knew.y) : "memory");
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(vb + off), "r"(vnew.x), "r"(vnew.y) : "memory");
+            const int64_t slot = (int64_t)page * kPageSize + r;
+            const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane;
+            *reinterpret_cast<uint2*>(p.K + dst) = knew;
+            *reinterpret_cast<uint2*>(p.V + dst) = vnew;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
+            __syncwarp();
+        }
 
         // ---- S = K q^T (two accumulators for ILP)
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -449,7 +705,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             sv[k] += __shfl_xor_sync(kFull, sv[k], 2);  // head column + remainder column
         }
         // sv[0]: (pos gid, head A), sv[1]: (gid, B), sv[2]: (gid+8, A), sv[3]: (gid+8, B)
-        const int pbase = (pg0 + i) * kPageSize + 16 * warp;
+        const int pbase = jj * kPageSize + 16 * warp;
         if (pbase + gid >= len) sv[0] = sv[1] = -CUDART_INF_F;
         if (pbase + gid + 8 >= len) sv[2] = sv[3] = -CUDART_INF_F;
 
@@ -514,157 +770,216 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * st);
-    }
-    if (!ok) {
-        if (lane == 0) {
-            atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-        }
-    }
-
-    // ---- per-warp finish: full sums over the warp's positions, head + remainder columns
-#pragma unroll
-    for (int o2 = 4; o2 < 32; o2 <<= 1) {
-        lA += __shfl_xor_sync(kFull, lA, o2);
-        lB += __shfl_xor_sync(kFull, lB, o2);
-    }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[mt][k] += __shfl_xor_sync(kFull, o[mt][k], 2);
-
-    float* sO = reinterpret_cast<float*>(sbase + L::kMergeO);
-    float* sM = reinterpret_cast<float*>(sbase + L::kMergeM);
-    float* sL = reinterpret_cast<float*>(sbase + L::kMergeL);
-    if (tig < 2) {
-        const int hA = 2 * tig, hB = hA + 1;
-        float* oA = sO + (warp * 4 + hA) * kHeadDim;
-        float* oB = sO + (warp * 4 + hB) * kHeadDim;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int d = 16 * mt + gid;
-            oA[d] = o[mt][0];
-            oB[d] = o[mt][1];
-            oA[d + 8] = o[mt][2];
-            oB[d + 8] = o[mt][3];
-        }
-        if (gid == 0) {
-            sM[warp * 4 + hA] = mA;
-            sM[warp * 4 + hB] = mB;
-            sL[warp * 4 + hA] = lA;
-            sL[warp * 4 + hB] = lB;
-        }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    if (*abort_flag) return;
-
-    // ---- merge the four warps: thread -> (head h, dims 4c..4c+3)
-    {
-        const int h = tid >> 5, c = tid & 31;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sM[w * 4 + h]);
-        float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = sM[w * 4 + h];
-            const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
-            Ls += f * sL[w * 4 + h];
-            const float4 ow = *reinterpret_cast<const float4*>(sO + (w * 4 + h) * kHeadDim + 4 * c);
-            acc[0] += f * ow.x;
-            acc[1] += f * ow.y;
-            acc[2] += f * ow.z;
-            acc[3] += f * ow.w;
-        }
-        const float inv = 1.f / Ls;
-        const int qh = g * kGroup + h;
-        if (nsplit == 1) {
-            const float y[4] = {acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv};
-            *reinterpret_cast<uint2*>(p.out + ((int64_t)t * H + qh) * kHeadDim + 4 * c) = pack4(y);
+        if (!(flags & kFlagLast)) {
+            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
         } else {
-            const int64_t ph = ((int64_t)t * H + qh) * p.max_splits + s;
-            *reinterpret_cast<float4*>(p.part_o + ph * kHeadDim + 4 * c) =
-                make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-            if (c == 0) p.part_lse[ph] = M + log2f(Ls);
+            // ---- end of segment: merge the four warps in a fixed order, write the output or a partial.
+            // Each warp parks its unscaled O in the K rows of this stage that only it read
+            // (rows 16w..16w+15 of the first half: 2 KiB), its m and l in sM/sL.
+            float lAs = lA, lBs = lB;
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                lAs += __shfl_xor_sync(kFull, lAs, o2);
+                lBs += __shfl_xor_sync(kFull, lBs, o2);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) o[mt][k] += __shfl_xor_sync(kFull, o[mt][k], 2);
+            float* park = reinterpret_cast<float*>(sbase + st * kStageBytes);  // [4 warps][4 heads][128]
+            if (tig < 2) {
+                const int hA = 2 * tig, hB = hA + 1;
+                float* pa = park + (warp * 4 + hA) * kHeadDim;
+                float* pb = park + (warp * 4 + hB) * kHeadDim;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int d = 16 * mt + gid;
+                    pa[d] = o[mt][0];
+                    pb[d] = o[mt][1];
+                    pa[d + 8] = o[mt][2];
+                    pb[d + 8] = o[mt][3];
+                }
+                if (gid == 0) {
+                    sM[warp * 4 + hA] = mA;
+                    sM[warp * 4 + hB] = mB;
+                    sL[warp * 4 + hA] = lAs;
+                    sL[warp * 4 + hB] = lBs;
+                }
+            }
+            if (!group_sync(bar_group, gphase, lane)) {
+                ok = false;
+                break;
+            }
+            {
+                const int h = warp;  // thread -> (head h, dims 4*lane..4*lane+3)
+                float M = -CUDART_INF_F;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sM[w * 4 + h]);
+                float Ls = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {  // fixed order: the result is reproducible
+                    const float mw = sM[w * 4 + h];
+                    const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+                    Ls += f * sL[w * 4 + h];
+                    const float4 ow = *reinterpret_cast<const float4*>(park + (w * 4 + h) * kHeadDim + 4 * lane);
+                    y[0] += f * ow.x;
+                    y[1] += f * ow.y;
+                    y[2] += f * ow.z;
+                    y[3] += f * ow.w;
+                }
+                const float inv = 1.f / Ls;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) y[k] *= inv;
+                const int qh = g * kGroup + h;
+                if (flags & kFlagComplete) {
+                    if (!(flags & kFlagValid)) y[0] = y[1] = y[2] = y[3] = 0.f;
+                    *reinterpret_cast<uint2*>(p.out + ((int64_t)t * H + qh) * kHeadDim + 4 * lane) = pack4(y);
+                } else {
+                    const int64_t ph = (int64_t)pidx * kGroup + h;
+                    *reinterpret_cast<float4*>(p.part_o + ph * kHeadDim + 4 * lane) =
+                        make_float4(y[0], y[1], y[2], y[3]);
+                    if (lane == 0) p.part_lse[ph] = M + log2f(Ls);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
+            if (!group_sync(bar_group, gphase, lane)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
         }
+    }
+    if (!ok && lane == 0) {
+        atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
     }
 }
 
-constexpr int kDecodeStages = 3;
+constexpr int kAttnStages = 3;
+
+int attn_ctas_per_sm()
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<kAttnStages>, kAttnThreads,
+                                                      AttnSmem<kAttnStages>::kAlloc) != cudaSuccess)
+        return 0;
+    return n;
+}
 
 cudaError_t configure_kernels()
 {
-    return cudaFuncSetAttribute(attn_decode_kernel<kDecodeStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                AttnSmem<kDecodeStages>::kAlloc);
+    return cudaFuncSetAttribute(attn_kernel<kAttnStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                AttnSmem<kAttnStages>::kAlloc);
 }
 
-cudaError_t launch_attn_decode(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
+cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& plan, bool decode_mode, bool pdl,
+                        cudaStream_t s)
 {
-    using L = AttnSmem<kDecodeStages>;
     AttnParams p;
-    p.qhat = reinterpret_cast<const float*>(a.ws + plan.off_qhat);
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.k = static_cast<const __nv_bfloat16*>(a.k);
+    p.v = static_cast<const __nv_bfloat16*>(a.v);
+    p.qw = static_cast<const __nv_bfloat16*>(a.q_norm_w);
+    p.kw = static_cast<const __nv_bfloat16*>(a.k_norm_w);
+    p.positions = a.step_positions;
     p.tok_len = reinterpret_cast<const int32_t*>(a.ws + plan.off_len);
     p.tok_row = reinterpret_cast<const int32_t*>(a.ws + plan.off_row);
     p.table = a.table;
-    p.pages = a.pages;
-    p.chunk = plan.chunk;
-    p.max_splits = plan.max_splits;
-    p.heads = pool->cfg.heads;
-    p.kv_heads = pool->cfg.kv_heads;
+    p.rope_hi = pool->rope_hi;
+    p.rope_lo = pool->rope_lo;
+    p.K = static_cast<__nv_bfloat16*>(pool->k);
+    p.V = static_cast<__nv_bfloat16*>(pool->v);
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.part_o = reinterpret_cast<float*>(a.ws + plan.off_po);
     p.part_lse = reinterpret_cast<float*>(a.ws + plan.off_plse);
+    p.prefix = reinterpret_cast<int32_t*>(a.ws + plan.off_prefix);
+    p.unit_ok = reinterpret_cast<int32_t*>(a.ws + plan.off_unit_ok);
     p.err = pool->err;
+    p.ntok = plan.tokens;
+    p.pages = a.pages;
+    p.num_pages = pool->num_pages;
+    p.max_seq = pool->cfg.max_seq;
+    p.heads = pool->cfg.heads;
+    p.kv_heads = pool->cfg.kv_heads;
+    p.decode_mode = decode_mode ? 1 : 0;
+    p.num_slots = pool->num_slots;
+    p.eps = static_cast<float>(pool->cfg.eps);
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)plan.tokens * pool->cfg.kv_heads * plan.max_splits));
+    cfg.gridDim = dim3((unsigned)plan.ctas);
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.dynamicSmemBytes = AttnSmem<kAttnStages>::kAlloc;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<kDecodeStages>, pool->tmap_k, pool->tmap_v, p);
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<kAttnStages>, pool->tmap_k, pool->tmap_v, p);
 }
 
 // =====================================================================================
-// G3: log-sum-exp combine of the splits
+// combine_kernel
 // =====================================================================================
 struct CombineParams {
-    const int32_t* tok_len;
-    int chunk, max_splits, heads;
+    const int32_t* prefix;    // [ntok + 1]
+    const int32_t* unit_ok;   // [U]
+    const int32_t* positions; // decode mode: [ntok]
     const float* part_o;
     const float* part_lse;
     __nv_bfloat16* out;
+    uint32_t* err;
+    int ntok, heads, kv_heads, ctas, decode_mode;
 };
 
-// One warp per (token, query head); lane owns dims 4*lane..4*lane+3.
-//   out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M)
+// CTA c of C (C <= T) covers global pages [c*T/C, (c+1)*T/C); the CTA holding page x.
+__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int C)
+{
+    int c = (int)(x * C / T);
+    while (c + 1 < C && (int64_t)(c + 1) * T / C <= x) ++c;
+    while (c > 0 && (int64_t)c * T / C > x) --c;
+    return c;
+}
+
+// One CTA per (token, kv head) unit; warp w = query head 4g+w, lane owns dims 4*lane..4*lane+3.
+//   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M)   over the unit's pieces c
 __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hq = p.heads / 4;
-    const int t = blockIdx.x / hq;
-    const int h = (blockIdx.x % hq) * 4 + warp;
+    const int G = p.kv_heads;
+    const int u = blockIdx.x;
+    const int t = u / G, g = u % G;
+    const int h = g * kGroup + warp;
     pdl_wait();
-    const int len = p.tok_len[t];
-    if (len == 0) return;
-    const int npg = (len + kPageSize - 1) / kPageSize;
-    const int nsplit = (npg + p.chunk - 1) / p.chunk;
-    if (nsplit <= 1) return;
-    const int64_t ph = ((int64_t)t * p.heads + h) * p.max_splits;
-    const float* lse = p.part_lse + ph;
+    __nv_bfloat16* dst = p.out + ((int64_t)t * p.heads + h) * kHeadDim + 4 * lane;
+    const int pre = p.prefix[t];
+    const int n = p.prefix[t + 1] - pre;
+    if (n == 0) {  // skipped token
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        if (p.decode_mode && g == 0 && threadIdx.x == 0) {
+            const int pos = p.positions[t];
+            if (pos != -1) atomicOr(p.err, PKV_DEVERR_POSITION);
+        }
+        return;
+    }
+    if (!p.unit_ok[u]) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        return;
+    }
+    const int64_t T = (int64_t)G * p.prefix[p.ntok];
+    const int Ce = (int)min((int64_t)p.ctas, T);  // the slices the attention kernel used
+    const int64_t S = (int64_t)G * pre + (int64_t)g * n;
+    const int64_t rf = cta_of(S, T, Ce), rl = cta_of(S + n - 1, T, Ce);
+    if (rf == rl) return;  // one CTA held the whole unit and wrote it out
     float M = -CUDART_INF_F;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, lse[s]);
+    for (int64_t r = rf + lane; r <= rl; r += 32) M = fmaxf(M, p.part_lse[((int64_t)u + r) * kGroup + warp]);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
     float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < nsplit; ++s) {
-        const float w = exp2f(lse[s] - M);
-        const float4 o = *reinterpret_cast<const float4*>(p.part_o + (ph + s) * kHeadDim + 4 * lane);
+    for (int64_t r = rf; r <= rl; ++r) {
+        const int64_t ph = ((int64_t)u + r) * kGroup + warp;
+        const float w = exp2f(p.part_lse[ph] - M);
+        const float4 o = *reinterpret_cast<const float4*>(p.part_o + ph * kHeadDim + 4 * lane);
         wsum += w;
         acc[0] += w * o.x;
         acc[1] += w * o.y;
@@ -673,22 +988,27 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
     }
     const float inv = 1.f / wsum;
     const float y[4] = {acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv};
-    *reinterpret_cast<uint2*>(p.out + ((int64_t)t * p.heads + h) * kHeadDim + 4 * lane) = pack4(y);
+    *reinterpret_cast<uint2*>(dst) = pack4(y);
 }
 
-cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
+cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& plan, bool decode_mode,
+                           cudaStream_t s)
 {
-    if (plan.max_splits <= 1) return cudaSuccess;
     CombineParams p;
-    p.tok_len = reinterpret_cast<const int32_t*>(a.ws + plan.off_len);
-    p.chunk = plan.chunk;
-    p.max_splits = plan.max_splits;
-    p.heads = pool->cfg.heads;
+    p.prefix = reinterpret_cast<const int32_t*>(a.ws + plan.off_prefix);
+    p.unit_ok = reinterpret_cast<const int32_t*>(a.ws + plan.off_unit_ok);
+    p.positions = a.step_positions;
     p.part_o = reinterpret_cast<const float*>(a.ws + plan.off_po);
     p.part_lse = reinterpret_cast<const float*>(a.ws + plan.off_plse);
     p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.err = pool->err;
+    p.ntok = plan.tokens;
+    p.heads = pool->cfg.heads;
+    p.kv_heads = pool->cfg.kv_heads;
+    p.ctas = plan.ctas;
+    p.decode_mode = decode_mode ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(plan.tokens * (pool->cfg.heads / 4)));
+    cfg.gridDim = dim3((unsigned)((int64_t)plan.tokens * pool->cfg.kv_heads));
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;

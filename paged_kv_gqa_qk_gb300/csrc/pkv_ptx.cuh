@@ -60,6 +60,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     return false;
 }
 
+// Bounded wait without sleeping, for short waits among the warps of one CTA
+// (try_wait itself suspends the thread for a while when the phase is open).
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t it = 0; it < (1u << 26); ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
 // ---- TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {

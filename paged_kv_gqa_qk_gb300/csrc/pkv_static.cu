@@ -1,7 +1,7 @@
 // pkv_decode_static: decode_paged for callers that cannot allocate device
 // memory.  The scratch that pkv_decode takes from the caller's workspace comes
 // from a fixed array compiled into this file instead; the call allocates
-// nothing and otherwise runs the same three kernels as pkv_decode.
+// nothing and otherwise enqueues the same kernels as pkv_decode.
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -46,8 +46,8 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
 {
     if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !table || !out) return PKV_EINVAL;
     if (rows <= 0 || pages <= 0) return PKV_EINVAL;
-    if (rows > (1 << 24) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
-    if (!aligned_to(q, 8) || !aligned_to(k, 8) || !aligned_to(v, 8) || !aligned_to(out, 8) ||
+    if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(out, 8) ||
         !aligned_to(q_norm_w, 8) || !aligned_to(k_norm_w, 8) || !aligned_to(positions, 4) || !aligned_to(table, 4))
         return PKV_EINVAL;
     const pkv::Plan plan = pkv::make_plan(pool, rows, pages);
@@ -58,11 +58,7 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
     const int rc = scratch_address(dev, &scratch);
     if (rc != PKV_OK) return rc;
 
-    pkv::StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
-                       0, rows, pages, out, static_cast<char*>(scratch)};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pkv::launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
-    if (pkv::launch_attn_decode(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
-    if (pkv::launch_combine(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
-    return PKV_OK;
+    const pkv::StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
+                             0, rows, pages, out, static_cast<char*>(scratch)};
+    return pkv::enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
 }

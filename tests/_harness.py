@@ -12,13 +12,13 @@ MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
 
-def run_gpu(wl: W.Workload, split_pages: int = 0, explicit_slots=None, table=None, step_positions=None,
+def run_gpu(wl: W.Workload, ctas: int = 0, explicit_slots=None, table=None, step_positions=None,
             positions=None, repeat: int = 1):
     dev = torch.device("cuda")
     K, V = wl.K0.to(dev), wl.V0.to(dev)
     pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
-    if split_pages:
-        pkv.pkv_set_split_pages(pool.handle, split_pages)
+    if ctas:
+        pkv.pkv_set_ctas(pool.handle, ctas)
     q, k, v, qw, kw = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w))
     tab = (wl.table if table is None else torch.as_tensor(table)).to(dev)
     sp = (wl.step_positions if step_positions is None else torch.as_tensor(step_positions)).to(dev)

@@ -62,7 +62,7 @@ def test_null_arguments_are_rejected(lib):
     assert lib.pkv_pool_free(None) == pkv.PKV_OK
     assert lib.pkv_pool_kv(None, None, None, None) == pkv.PKV_EINVAL
     assert lib.pkv_check_errors(None, None, None) == pkv.PKV_EINVAL
-    assert lib.pkv_set_split_pages(None, 0) == pkv.PKV_EINVAL
+    assert lib.pkv_set_ctas(None, 0) == pkv.PKV_EINVAL
     assert lib.pkv_timer_enable(None, 1) == pkv.PKV_EINVAL
     assert lib.pkv_config_default(None) == pkv.PKV_EINVAL
     out = vp()

@@ -22,10 +22,10 @@ pytestmark = pytest.mark.gpu
 
 # ------------------------------------------------------------------ the five configurations
 
-@pytest.mark.parametrize("split", [0, 1, 2])
-def test_config1_tiny(split):
+@pytest.mark.parametrize("ctas", [0, 1, 2, 5])
+def test_config1_tiny(ctas):
     wl = W.config1()
-    ma, rel = compare(wl, run_gpu(wl, split_pages=split), run_oracle(wl), label=f"config1 split={split}")
+    ma, rel = compare(wl, run_gpu(wl, ctas=ctas), run_oracle(wl), label=f"config1 ctas={ctas}")
     assert ma < 5e-3
 
 
@@ -55,15 +55,15 @@ def test_config5_step_mix():
     compare(wl, run_gpu(wl), run_oracle(wl, sel=sel), sel=sel, label="config5")
 
 
-# ------------------------------------------------------------------ tiles, ragged tails, split sizes
+# ------------------------------------------------------------------ tiles, ragged tails, partitions
 
 RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 191, 640, 1000, 4097]
 
 
-@pytest.mark.parametrize("split", [0, 1, 3, 7])
-def test_ragged_lengths_and_split_sizes(split):
+@pytest.mark.parametrize("ctas", [0, 1, 3, 7, 1000])
+def test_ragged_lengths_and_partitions(ctas):
     wl = W.make_decode("ragged", RAGGED, seed=77, table_pages=70)
-    compare(wl, run_gpu(wl, split_pages=split), run_oracle(wl), label=f"ragged split={split}")
+    compare(wl, run_gpu(wl, ctas=ctas), run_oracle(wl), label=f"ragged ctas={ctas}")
 
 
 def test_sweep_shape_small():
@@ -78,7 +78,30 @@ def test_step_small_with_explicit_slots():
     ref = run_oracle(wl)
     compare(wl, run_gpu(wl, explicit_slots=slots), ref, label="step explicit slots")
     compare(wl, run_gpu(wl), ref, label="step derived slots")
-    compare(wl, run_gpu(wl, split_pages=1), ref, label="step split=1")
+    compare(wl, run_gpu(wl, ctas=1), ref, label="step ctas=1")
+    compare(wl, run_gpu(wl, ctas=13), ref, label="step ctas=13")
+
+
+@pytest.mark.parametrize("ctas", [0, 7])
+def test_new_key_dominates(ctas):
+    """Each row's new key equals its first query head's (same raw vector, same
+    norm weight, same position), so that head puts ~99% of its weight on the
+    key the call has just written.  A read of the page before the write would
+    miss it and be off by O(1), far outside the tolerance."""
+    wl = W.make_decode("own key", [1000, 1, 65, 130, 2049, 64], seed=26, table_pages=33)
+    k = wl.k.clone()
+    for g in range(wl.cfg["kv_heads"]):
+        k[:, g] = wl.q[:, 4 * g]
+    wl = W.Workload(**{**wl.__dict__, "k": k, "k_norm_w": wl.q_norm_w.clone()})
+    gpu, ref = run_gpu(wl, ctas=ctas), run_oracle(wl)
+    compare(wl, gpu, ref, label=f"own key ctas={ctas}")
+    # the new key's value dominates the first head of every group
+    S = wl.cfg["page_size"]
+    vnew = wl.v.double().numpy()
+    out = ref[0]
+    for b, L in enumerate(wl.meta["lengths"]):
+        for g in range(wl.cfg["kv_heads"]):
+            assert np.abs(out[b, 4 * g] - vnew[b, g]).max() < 0.1 * max(1.0, np.abs(vnew[b, g]).max())
 
 
 def test_repeated_calls_are_idempotent():
@@ -158,7 +181,8 @@ def test_kv_head_shards_reproduce_full_result():
     library once per kv-head shard (a pool of kv_heads/n heads, the matching
     query heads) and concatenating reproduces the full result bit-exactly."""
     wl = W.make_decode("shard", [500, 64, 1300, 7], seed=25, table_pages=24)
-    full = run_gpu(wl, split_pages=4)
+    # one CTA: every (token, kv head) is summed in the same order whatever the shard
+    full = run_gpu(wl, ctas=1)
     n = 4
     G = wl.cfg["kv_heads"] // n
     outs = []
@@ -168,7 +192,7 @@ def test_kv_head_shards_reproduce_full_result():
         part = W.Workload(wl.name, cfg, wl.num_pages, wl.K0[g0:g1].contiguous(), wl.V0[g0:g1].contiguous(),
                           wl.q[:, 4 * g0:4 * g1].contiguous(), wl.k[:, g0:g1].contiguous(),
                           wl.v[:, g0:g1].contiguous(), wl.q_norm_w, wl.k_norm_w, wl.table, wl.step_positions)
-        out, K, V, flags = run_gpu(part, split_pages=4)
+        out, K, V, flags = run_gpu(part, ctas=1)
         assert flags == 0
         assert torch.equal(K, full[1][g0:g1]) and torch.equal(V, full[2][g0:g1])
         outs.append(out)
