@@ -199,7 +199,7 @@ PKV_API int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void*
  *   slots          device int32 [P], or NULL: derive each slot from the table
  *   step_positions device int32 [rows]; -1 = row takes no step
  *   table          device int32 [rows][pages]
- *   out            device bf16 [P + rows][heads][head_dim] (prompts, then steps)
+ *   out            device bf16 [P + rows][heads][head_dim] (prompts, then steps), 16-byte aligned
  *   workspace      >= pkv_workspace_bytes(pool, rows, pages, P)
  * The pages require P > 0 and rows > 0 (PKV_EINVAL otherwise).  Slots must
  * be distinct as for pkv_decode; every write of the call is ordered before

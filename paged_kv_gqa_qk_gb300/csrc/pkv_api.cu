@@ -50,21 +50,37 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
     return pl;
 }
 
+// decode: attention (which also validates rows and appends their k/v) -> combine.
+// step:   prep (validates every token, appends every k/v) -> prompt-token
+//         attention on the tensor cores -> step-row attention -> combine.
+// All but the first kernel use programmatic dependent launch: each is
+// scheduled while the one before it drains and waits for it before touching
+// memory.
 int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
 {
     const bool decode = a.P == 0;
-    if (!decode && launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+    StepArgs as = a;  // the tokens the attention + combine kernels see
+    Plan ps = plan;
+    if (!decode) {
+        if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+        if (launch_prefill(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+        // the step rows are tokens P..P+rows-1
+        const size_t qrow = (size_t)pool->cfg.heads * pool->cfg.head_dim * 2;
+        as.q = static_cast<const char*>(a.q) + (size_t)a.P * qrow;
+        as.out = static_cast<char*>(a.out) + (size_t)a.P * qrow;
+        ps.tokens = a.rows;
+        ps.off_len += sizeof(int32_t) * a.P;
+        ps.off_row += sizeof(int32_t) * a.P;
+    }
     const bool timed = pool->timer_on;
     const int slot = (int)(pool->timer_count % kTimerSlots);
     if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
-    // programmatic dependent launch: the kernel is scheduled while the one
-    // before it drains, and waits for it before touching memory
-    if (launch_attn(pool, a, plan, decode, !timed, s) != cudaSuccess) return PKV_ECUDA;
+    if (launch_attn(pool, as, ps, decode, !timed, s) != cudaSuccess) return PKV_ECUDA;
     if (timed) {
         if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
         pool->timer_count++;
     }
-    if (launch_combine(pool, a, plan, decode, s) != cudaSuccess) return PKV_ECUDA;
+    if (launch_combine(pool, as, ps, decode, s) != cudaSuccess) return PKV_ECUDA;
     return PKV_OK;
 }
 
@@ -191,6 +207,7 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
     ok &= make_tmap(&p->tmap_k, p->k, num_slots, cfg->kv_heads);
     ok &= make_tmap(&p->tmap_v, p->v, num_slots, cfg->kv_heads);
     ok &= configure_kernels() == cudaSuccess;
+    ok &= configure_prefill() == cudaSuccess;
     p->ctas_per_sm = attn_ctas_per_sm();
     ok &= p->ctas_per_sm > 0;
     if (!ok) {
@@ -329,7 +346,7 @@ int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const 
         return PKV_EINVAL;
     if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
     if ((int64_t)P + rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(q_norm_w, 8) ||
         !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(prow, 4) || !aligned(step_positions, 4) ||
         !aligned(table, 4) || (slots && !aligned(slots, 4)))
         return PKV_EINVAL;

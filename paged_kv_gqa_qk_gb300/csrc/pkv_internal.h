@@ -79,6 +79,7 @@ struct StepArgs {
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.
 cudaError_t configure_kernels();
+cudaError_t configure_prefill();
 // Resident attention CTAs per SM (0 on error).
 int attn_ctas_per_sm();
 
@@ -90,6 +91,8 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
                         cudaStream_t s);
 cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& plan, bool decode_mode,
                            cudaStream_t s);
+// step mode: prompt-token attention on tcgen05 tensor cores (pkv_prefill.cu)
+cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
 
 // Enqueue one decode (a.P == 0) or step call on workspace a.ws; host checks done.
 int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
