@@ -77,6 +77,10 @@ def make_workload(name: str, rank: int = 0):
     elif name == "config4":
         wl = W.make_decode("shared-prefix decode 256 rows x U[1024,8192], groups of 16 share 8-32 pages",
                            (256, 1024, 8192), seed=rank_seed(1004, rank), table_pages=128, share_groups=16)
+    elif name == "config5":
+        wl = W.config5() if rank == 0 else None
+        if wl is None:
+            raise SystemExit("config5 runs on one rank")
     elif name.startswith("sweep"):
         r, l = name[5:].split("x")
         wl = W.sweep(int(r), int(l), seed=rank_seed(2000 + int(r) + int(l), rank))
@@ -181,7 +185,7 @@ def attention_algorithmic_bytes(wl) -> int:
     read, then written to the pool) and its bf16 output."""
     import workloads as W
     S = wl.cfg["page_size"]
-    L = [int(p) + 1 for p in wl.step_positions.tolist() if p >= 0]
+    L = [int(p) + 1 for p in wl.step_positions.tolist() if p >= 0]  # the rows the attention kernel serves
     kv = W.kv_bytes_per_position(wl.cfg) * sum(L)
     table = 4 * sum(-(-x // S) for x in L)
     H, G, D = wl.cfg["heads"], wl.cfg["kv_heads"], wl.cfg["head_dim"]
@@ -206,18 +210,24 @@ def run_gpu(args) -> None:
     pkv.load_library()
 
     wl = make_workload(args.workload, rank)
-    R, pages = wl.R, wl.pages
+    R, pages, P = wl.R, wl.pages, wl.P
     K, V = wl.K0.to(dev), wl.V0.to(dev)
     pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
     q, k, v, qw, kw, pos, tab = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w,
                                                     wl.step_positions, wl.table))
     out = torch.empty_like(q)
-    ws = pool.workspace(R, pages, 0)
+    ws = pool.workspace(R, pages, P)
     stream = torch.cuda.Stream(device=dev)
-    nsplit_gt1 = True  # combine launches whenever the plan has more than one split column
+    if wl.kind == "decode":
+        def step():
+            pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, out, ws, stream)
+        launches_per_step = 2   # attention, combine
+    else:  # step_paged: prompt chunks + one step per row
+        ppos, prow = wl.positions.to(dev), wl.prow.to(dev)
 
-    def step():
-        pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, out, ws, stream)
+        def step():
+            pkv.pkv_step(pool.handle, q, k, v, qw, kw, ppos, prow, None, pos, tab, out, ws, stream)
+        launches_per_step = 4   # prep, prompt attention, step-row attention, combine
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -256,6 +266,9 @@ def run_gpu(args) -> None:
     # memory and the output D2H, every step, inside the timed region
     host_in = [t.pin_memory() for t in (wl.q, wl.k, wl.v, wl.step_positions, wl.table)]
     dev_in = [q, k, v, pos, tab]
+    if wl.kind == "step":
+        host_in += [wl.positions.pin_memory(), wl.prow.pin_memory()]
+        dev_in += [ppos, prow]
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out.numel() * host_out.element_size()
@@ -280,8 +293,7 @@ def run_gpu(args) -> None:
     achieved = plan_bytes / attn_avg_s / 1e9
     peak, peak_kind = measured_peak_hbm()
     logical = wl.meta["logical_kv_bytes"]
-    launches_per_step = 3
-    rows_total = R * world
+    rows_total = (R + P) * world  # tokens attended per step (decode: rows)
     res = {
         "metric": METRIC,
         "value": rows_total / (ms_step / 1e3),
@@ -295,9 +307,11 @@ def run_gpu(args) -> None:
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v/cache, U[0.5,1.5] norm weights, shuffled pages)",
-        "config": {"workload": wl.name, "rows": R, "table_pages": pages, "pool_pages": wl.num_pages,
+        "config": {"workload": wl.name, "rows": R, "prompt_tokens": P, "table_pages": pages,
+                   "pool_pages": wl.num_pages,
                    "heads": wl.cfg["heads"], "kv_heads": wl.cfg["kv_heads"], "head_dim": wl.cfg["head_dim"],
-                   "page_size": wl.cfg["page_size"], "sum_context": sum(wl.meta["lengths"]),
+                   "page_size": wl.cfg["page_size"],
+                   "sum_context": sum(wl.meta.get("lengths", wl.meta.get("decode_lengths", []))),
                    "kv_bytes_per_step": logical,
                    "l2": f"inputs larger than L2: {logical / 1e9:.2f} GB of K/V per step vs 126 MB L2",
                    "parallelism": f"dp{world} (independent replicas, rows sharded by rank)"},
@@ -312,7 +326,7 @@ def run_gpu(args) -> None:
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.kind == "decode":
         res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     pool.close()
     if rank == 0:

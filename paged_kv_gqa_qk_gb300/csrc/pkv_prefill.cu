@@ -320,20 +320,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 tc_fence_after();
                 float s[kPageSize];
-#pragma unroll
-                for (int c = 0; c < kPageSize; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tl + sb * kPageSize + c, v);
+                {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tl + sb * kPageSize, v0);
+                    tmem_ld32(tl + sb * kPageSize + 32, v1);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) s[c + e] = __uint_as_float(v[e]);
+                    for (int c = 0; c < 32; ++c) {
+                        s[c] = __uint_as_float(v0[c]);
+                        s[c + 32] = __uint_as_float(v1[c]);
+                    }
                 }
-                float mx = -CUDART_INF_F;
+                // causal mask: keys up to pos; only a page that reaches past pos needs it
+                const int first = jj * kPageSize;
+                if (!active || first > pos) {
 #pragma unroll
-                for (int c = 0; c < kPageSize; ++c) {
-                    if (!active || jj * kPageSize + c > pos) s[c] = -CUDART_INF_F;  // causal: keys up to pos
-                    mx = fmaxf(mx, s[c]);
+                    for (int c = 0; c < kPageSize; ++c) s[c] = -CUDART_INF_F;
+                } else if (first + kPageSize - 1 > pos) {
+#pragma unroll
+                    for (int c = 0; c < kPageSize; ++c)
+                        if (first + c > pos) s[c] = -CUDART_INF_F;
                 }
+                float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+                for (int c = 4; c < kPageSize; c += 4) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], s[c + e]);
+                }
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
                 // move the running max (rescaling O and l) only when this page raises it by > 8
                 bool need = false;
                 float alpha = 1.f;
@@ -366,16 +380,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
                 }
                 // P_j = 2^(S_j - m): into P buffer sb once the product two pages back has read it
-                float psum = 0.f;
+                // (a row with no key yet has m = -inf: its p are all 0)
+                const float msub = m_used == -CUDART_INF_F ? 0.f : m_used;
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t pk[kPageSize / 2];
 #pragma unroll
                 for (int c = 0; c < kPageSize; c += 2) {
-                    const float a = s[c] == -CUDART_INF_F ? 0.f : exp2f(s[c] - m_used);
-                    const float b = s[c + 1] == -CUDART_INF_F ? 0.f : exp2f(s[c + 1] - m_used);
-                    psum += a + b;
-                    pk[c / 2] = pack_bf16(__float2bfloat16_rn(a), __float2bfloat16_rn(b));
+                    const float a = ex2_approx(s[c] - msub);
+                    const float b = ex2_approx(s[c + 1] - msub);
+                    ps4[(c >> 1) & 3] += a + b;
+                    __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
+                    pk[c / 2] = *reinterpret_cast<uint32_t*>(&ab);
                 }
-                l += psum;
+                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
                 if (j >= 2 && !mbar_wait(bar_o + 8 * sb, ((j - 2) >> 1) & 1)) {
                     ok = false;
                     break;
