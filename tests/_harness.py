@@ -83,6 +83,7 @@ def compare(wl, gpu, ref, sel=None, label=""):
     max_abs = float(np.abs(got - rout).max()) if got.size else 0.0
     nrm = float(np.linalg.norm(rout))
     rel = float(np.linalg.norm(got - rout) / nrm) if nrm > 0 else float(np.linalg.norm(got))
+    print(f"[parity] {label}: max-abs {max_abs:.3e} rel-L2 {rel:.3e}")
     assert max_abs <= MAX_ABS, f"{label}: max-abs {max_abs:.3e} > {MAX_ABS}"
     assert rel <= REL_L2, f"{label}: rel-L2 {rel:.3e} > {REL_L2}"
     return max_abs, rel
