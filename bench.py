@@ -8,7 +8,8 @@ Qwen3-8B attention shapes (32 query heads, 8 kv heads, head_dim 128, pages of
 implies), with the attention kernel's achieved HBM bandwidth against the
 measured copy bandwidth of the chip.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload config2|config3|config4|sweepRxL]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--workload config2|config3|config4|config5|sweepRxL|prefill|rows]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch of the
@@ -32,6 +33,9 @@ if ROOT not in sys.path:
 
 METRIC = "decode_paged rows/s and KV-read GB/s vs GB300 HBM roofline (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 126 << 20          # L2 of one GB300 as the driver reports it
+L2_FLUSH_BYTES = 512 << 20
 
 
 # ---------------------------------------------------------------------------- distributed helpers
@@ -81,6 +85,10 @@ def make_workload(name: str, rank: int = 0):
         wl = W.config5() if rank == 0 else None
         if wl is None:
             raise SystemExit("config5 runs on one rank")
+    elif name == "prefill":
+        wl = W.prefill_mix(seed=rank_seed(1006, rank))
+    elif name == "rows":
+        wl = W.rows_mix(seed=rank_seed(1007, rank))
     elif name.startswith("sweep"):
         r, l = name[5:].split("x")
         wl = W.sweep(int(r), int(l), seed=rank_seed(2000 + int(r) + int(l), rank))
@@ -158,6 +166,22 @@ def measured_peak_hbm():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_peak_bf16():
+    """Dense bf16 tensor TFLOP/s (burst) from the measured peaks, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        for key in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+            if key in d:
+                v = d[key]
+                v = v.get("value", v) if isinstance(v, dict) else v
+                return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     with open(os.path.join(ROOT, "paged_kv_gqa_qk_gb300", "csrc", "pkv_kernels.cu"), "rb") as f:
@@ -176,6 +200,14 @@ def ncu_traffic(workload: str):
     if d.get("kernel_sha") != kernel_source_hash() or d.get("workload") != workload:
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def prefill_algorithmic_flops(wl) -> int:
+    """FLOPs the prompt-attention kernel must do per launch: for every prompt
+    token at position p and every query head, scores against p + 1 keys and
+    the weighted sum of p + 1 values, 2 * head_dim FLOPs each."""
+    H, D = wl.cfg["heads"], wl.cfg["head_dim"]
+    return sum(4 * H * D * (int(p) + 1) for p in wl.positions.tolist())
 
 
 def attention_algorithmic_bytes(wl) -> int:
@@ -213,21 +245,33 @@ def run_gpu(args) -> None:
     R, pages, P = wl.R, wl.pages, wl.P
     K, V = wl.K0.to(dev), wl.V0.to(dev)
     pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
-    q, k, v, qw, kw, pos, tab = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w,
+    # a prefill call takes the P prompt tokens only (its table rows take no step)
+    ntok = P if wl.kind == "prefill" else P + R
+    host_q, host_k, host_v = wl.q[:ntok], wl.k[:ntok], wl.v[:ntok]
+    q, k, v, qw, kw, pos, tab = (t.to(dev) for t in (host_q, host_k, host_v, wl.q_norm_w, wl.k_norm_w,
                                                     wl.step_positions, wl.table))
+    if wl.contiguous:
+        tab = None   # the library's contiguous-row layout, no table
     out = torch.empty_like(q)
-    ws = pool.workspace(R, pages, P)
+    ws = pool.workspace(0 if wl.kind == "prefill" else R, pages, P)
     stream = torch.cuda.Stream(device=dev)
     if wl.kind == "decode":
         def step():
-            pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, out, ws, stream)
+            pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, out, ws, stream, pages=pages)
         launches_per_step = 2   # attention, combine
-    else:  # step_paged: prompt chunks + one step per row
+    elif wl.kind == "step":  # step_paged: prompt chunks + one step per row
         ppos, prow = wl.positions.to(dev), wl.prow.to(dev)
 
         def step():
-            pkv.pkv_step(pool.handle, q, k, v, qw, kw, ppos, prow, None, pos, tab, out, ws, stream)
+            pkv.pkv_step(pool.handle, q, k, v, qw, kw, ppos, prow, None, pos, tab, out, ws, stream, pages=pages)
         launches_per_step = 4   # prep, prompt attention, step-row attention, combine
+    else:  # prefill_paged: prompt chunks only
+        ppos, prow = wl.positions.to(dev), wl.prow.to(dev)
+
+        def step():
+            pkv.pkv_prefill(pool.handle, q, k, v, qw, kw, ppos, prow, None, tab, out, ws, stream, rows=R,
+                            pages=pages)
+        launches_per_step = 2   # prep, prompt attention
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -241,22 +285,40 @@ def run_gpu(args) -> None:
     # as a user runs them (no events between the kernels, which would break
     # their programmatic overlap); pass 2 times the attention kernel alone
     # with events around each launch, for the roofline.
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Workloads whose K/V fit in L2 flush it (a write larger than L2, outside
+    # the timed events) before every timed step.
+    logical = wl.meta["logical_kv_bytes"]
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if logical < 2 * L2_BYTES else None
+
+    def flush():
+        if flush_buf is not None:
+            with torch.cuda.stream(stream):
+                flush_buf.zero_()
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 if flush_buf is None else 2 * args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
+        if flush_buf is None:
+            evs[0].record(stream)
+            for _ in range(args.steps):
+                step()
+            evs[1].record(stream)
+        else:
+            for i in range(args.steps):
+                flush()
+                evs[2 * i].record(stream)
+                step()
+                evs[2 * i + 1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
         pkv.pkv_timer_enable(pool.handle, True)
         for _ in range(args.steps):
+            flush()
             step()
         torch.cuda.synchronize()
     barrier(world)
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(len(evs) // 2))
     attn_ms, attn_n = pkv.pkv_timer_read(pool.handle)
     pkv.pkv_timer_enable(pool.handle, False)
     ms_total = max_over_ranks(ms_total, world)
@@ -264,9 +326,15 @@ def run_gpu(args) -> None:
 
     # ---- end-to-end through the C ABI with host buffers: inputs H2D from pinned
     # memory and the output D2H, every step, inside the timed region
-    host_in = [t.pin_memory() for t in (wl.q, wl.k, wl.v, wl.step_positions, wl.table)]
-    dev_in = [q, k, v, pos, tab]
-    if wl.kind == "step":
+    host_in = [t.pin_memory() for t in (host_q, host_k, host_v)]
+    dev_in = [q, k, v]
+    if wl.kind != "prefill":
+        host_in.append(wl.step_positions.pin_memory())
+        dev_in.append(pos)
+    if tab is not None:
+        host_in.append(wl.table.pin_memory())
+        dev_in.append(tab)
+    if wl.kind != "decode":
         host_in += [wl.positions.pin_memory(), wl.prow.pin_memory()]
         dev_in += [ppos, prow]
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -277,6 +345,7 @@ def run_gpu(args) -> None:
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
+            flush()
             for d, h in zip(dev_in, host_in):
                 d.copy_(h, non_blocking=True)
             step()
@@ -288,16 +357,30 @@ def run_gpu(args) -> None:
     if flags:
         raise SystemExit(f"device error flags {flags}")
 
-    plan_bytes = attention_algorithmic_bytes(wl)
     attn_avg_s = attn_ms / 1e3 / max(attn_n, 1)
-    achieved = plan_bytes / attn_avg_s / 1e9
-    peak, peak_kind = measured_peak_hbm()
-    logical = wl.meta["logical_kv_bytes"]
-    rows_total = (R + P) * world  # tokens attended per step (decode: rows)
+    timing = "CUDA events around each timed launch, second timed pass of the same steps"
+    if wl.kind == "prefill":
+        flops = prefill_algorithmic_flops(wl)
+        peak, peak_kind = measured_peak_bf16()
+        roofline = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": flops / attn_avg_s / 1e12,
+                    "peak": peak, "peak_kind": f"{peak_kind} (dense bf16 TFLOP/s, burst)", "unit": "TFLOP/s",
+                    "frac": flops / attn_avg_s / 1e12 / peak, "traffic": None,
+                    "algorithmic_flops_per_launch": flops, "avg_launch_us": attn_avg_s * 1e6,
+                    "timed_launches": attn_n, "timing": timing}
+    else:
+        plan_bytes = attention_algorithmic_bytes(wl)
+        achieved = plan_bytes / attn_avg_s / 1e9
+        peak, peak_kind = measured_peak_hbm()
+        roofline = {"bound": "hbm", "kernel": "attn_kernel", "achieved": achieved, "peak": peak,
+                    "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": ncu_traffic(args.workload), "algorithmic_bytes_per_launch": plan_bytes,
+                    "avg_launch_us": attn_avg_s * 1e6, "timed_launches": attn_n, "timing": timing}
+    rows_total = ntok * world  # tokens attended per step (decode: rows)
+    unit = "tokens/s" if wl.kind == "prefill" else "rows/s"
     res = {
         "metric": METRIC,
         "value": rows_total / (ms_step / 1e3),
-        "unit": "rows/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -313,15 +396,14 @@ def run_gpu(args) -> None:
                    "page_size": wl.cfg["page_size"],
                    "sum_context": sum(wl.meta.get("lengths", wl.meta.get("decode_lengths", []))),
                    "kv_bytes_per_step": logical,
-                   "l2": f"inputs larger than L2: {logical / 1e9:.2f} GB of K/V per step vs 126 MB L2",
+                   "l2": (f"inputs larger than L2: {logical / 1e9:.2f} GB of K/V per step vs 126 MB L2"
+                          if flush_buf is None else
+                          f"L2 flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the "
+                          f"device-timed events, inside the e2e time): {logical / 1e6:.0f} MB of K/V per step"),
                    "parallelism": f"dp{world} (independent replicas, rows sharded by rank)"},
         "kv_gbs": logical / (ms_step / 1e3) / 1e9 * world,
-        "roofline": {"bound": "hbm", "kernel": "attn_kernel", "achieved": achieved, "peak": peak,
-                     "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic(args.workload), "algorithmic_bytes_per_launch": plan_bytes,
-                     "avg_launch_us": attn_avg_s * 1e6, "timed_launches": attn_n,
-                     "timing": "CUDA events around each attention launch, second timed pass of the same steps"},
-        "e2e": {"value": rows_total * args.steps / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+        "roofline": roofline,
+        "e2e": {"value": rows_total * args.steps / e2e_s, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),

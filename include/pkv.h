@@ -27,9 +27,9 @@
  *   - "device" pointers must point into memory of the current CUDA device;
  *     "host" pointers into ordinary host memory.  The caller owns every
  *     tensor it passes; the library never frees them.
- *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  pkv_decode
- *     and pkv_step only enqueue work on it: they neither allocate nor
- *     synchronise, and return before the GPU has run.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  pkv_decode,
+ *     pkv_step and pkv_prefill only enqueue work on it: they neither allocate
+ *     nor synchronise, and return before the GPU has run.
  *   - Errors a host check can see (null pointers, sizes, a workspace that is
  *     too small, an unsupported configuration) are returned synchronously as
  *     negative PKV_E* codes and nothing is enqueued.  Errors that depend on
@@ -37,6 +37,13 @@
  *     device: the token is skipped (no write, zero output) and a bit is set
  *     in the pool's sticky error word, read with pkv_check_errors().  No
  *     kernel traps or spins without bound.
+ *   - Every `table` argument may be NULL: the contiguous-row layout of the
+ *     pages' non-paged entries (src/attention.linnet decode_rows,
+ *     prefill_packed, step_packed), where row b owns the `pages` pool pages
+ *     b * pages .. b * pages + pages - 1, so its position s sits at slot
+ *     b * pages * page_size + s.  It needs rows * pages <= num_pages
+ *     (PKV_ERANGE otherwise) and is otherwise the same as passing that
+ *     identity table.
  *   - The kernels are built for head_dim 128, page_size 64 and
  *     heads == 4 * kv_heads (Qwen3-8B: 32 query heads over 8 kv heads); other
  *     shapes are rejected with PKV_ENOTIMPL at pool creation.
@@ -138,7 +145,7 @@ PKV_API int pkv_pool_kv(const pkv_pool* pool, void** k, void** v, int64_t* num_s
 /* ---- workspace ------------------------------------------------------------------
  * Scratch device memory a call needs, in bytes, for `tokens = prefill_tokens +
  * rows` tokens and a page table `pages` wide.  The caller allocates it (256-byte
- * aligned) and passes it to pkv_decode / pkv_step; its contents need no
+ * aligned) and passes it to pkv_decode / pkv_step / pkv_prefill; its contents need no
  * initialisation and are not meaningful after the call.  The size depends
  * only on the pool (its config and attention grid size, see pkv_set_ctas),
  * rows and prefill_tokens: about 16.5 KiB per token plus 2 KiB per attention
@@ -165,7 +172,7 @@ PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int p
  *             zero output, not an error) -- the pages' own convention, a row
  *             that lists a scratch page, works as well
  *   table     device int32 [rows][pages], row-major; entries past a row's
- *             last page are never read
+ *             last page are never read.  NULL: contiguous rows (decode_rows)
  *   out       device bf16 [rows][heads][head_dim]
  *   workspace device, >= pkv_workspace_bytes(pool, rows, pages, 0), 256-byte aligned
  *
@@ -198,7 +205,7 @@ PKV_API int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void*
  *   prow           device int32 [P]    (the pages' `rows` argument)
  *   slots          device int32 [P], or NULL: derive each slot from the table
  *   step_positions device int32 [rows]; -1 = row takes no step
- *   table          device int32 [rows][pages]
+ *   table          device int32 [rows][pages], or NULL: contiguous rows (step_packed)
  *   out            device bf16 [P + rows][heads][head_dim] (prompts, then steps), 16-byte aligned
  *   workspace      >= pkv_workspace_bytes(pool, rows, pages, P)
  * The pages require P > 0 and rows > 0 (PKV_EINVAL otherwise).  Slots must
@@ -208,6 +215,33 @@ PKV_API int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v
              const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
              const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- prefill_paged -------------------------------------------------------------------
+ * qwen3-8b Nest files, src/attention.linnet GroupedQueryAttention.prefill_paged:
+ * P prompt tokens packed end to end, no step tokens.  Prompt token p sits at
+ * position positions[p] of table row prow[p] and is written at slots[p]; all
+ * P tokens are normed, roped and written first, then token p attends over
+ * table[prow[p]] for positions 0..positions[p].  A prompt may continue a row
+ * (a later chunk of a long prompt, or a prompt after a shared prefix whose
+ * pages the row lists): it sees every key the row already holds below its
+ * position as well as its own chunk's.
+ *
+ *   q          device bf16 [P][heads][head_dim], 16-byte aligned
+ *   k, v       device bf16 [P][kv_heads][head_dim]
+ *   positions  device int32 [P]
+ *   prow       device int32 [P]    (the pages' `rows` argument)
+ *   slots      device int32 [P], or NULL: derive each slot from the table
+ *   table      device int32 [rows][pages], or NULL: contiguous rows.  With a
+ *              NULL table and every prompt filling its own row from position 0,
+ *              this is prefill_packed with segments = prow.
+ *   out        device bf16 [P][heads][head_dim], 16-byte aligned
+ *   workspace  >= pkv_workspace_bytes(pool, 0, pages, P)
+ * P > 0 and rows > 0 (PKV_EINVAL otherwise); `rows` bounds prow[p].  Slots must
+ * be distinct; every write of the call is ordered before every read. */
+PKV_API int pkv_prefill(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+                        const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
+                        const int32_t* table, int P, int rows, int pages, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /* ---- decode without a caller workspace -------------------------------------------------------
  * The pages have no counterpart to this entry point; it is a convenience of
@@ -251,8 +285,8 @@ PKV_API int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags);
 PKV_API int pkv_set_ctas(pkv_pool* pool, int ctas);
 
 /* Kernel timer: while enabled, every pkv_decode / pkv_step records a pair of
- * CUDA events on its stream around the attention kernel (the dominant
- * launch).  pkv_timer_read synchronises on the last recorded event,
+ * CUDA events on its stream around the decode attention kernel (the dominant
+ * launch), and every pkv_prefill around its prompt-attention kernel.  pkv_timer_read synchronises on the last recorded event,
  * returns the summed duration in milliseconds and the number of timed
  * launches since the timer was last enabled, and keeps the timer running.
  * At most 4096 launches are kept (later ones overwrite the oldest). */

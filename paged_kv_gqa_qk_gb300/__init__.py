@@ -25,7 +25,7 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 
 # Every symbol include/pkv.h declares.
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
-               "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_check_errors",
+               "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_prefill", "pkv_check_errors",
                "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static")
 
 # Size of the scratch array pkv_decode_static uses in place of a workspace.
@@ -71,6 +71,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_workspace_bytes": ([vp, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "pkv_decode": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp], i32),
         "pkv_step": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp], i32),
+        "pkv_prefill": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp], i32),
         "pkv_check_errors": ([vp, vp, ctypes.POINTER(ctypes.c_uint32)], i32),
         "pkv_set_ctas": ([vp, i32], i32),
         "pkv_timer_enable": ([vp, i32], i32),
@@ -169,37 +170,65 @@ def pkv_workspace_bytes(pool, rows: int, pages: int, prefill_tokens: int = 0) ->
     return n.value
 
 
-def pkv_decode(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, workspace, stream=None) -> None:
-    rows, pages = int(table.shape[0]), int(table.shape[1])
+def _table(table, rows, pages):
+    """(pointer, rows, pages) of a page table, or of the contiguous-row layout when ``table`` is None."""
+    if table is None:
+        if rows is None or pages is None:
+            raise ValueError("without a table, rows and pages are required")
+        return ctypes.c_void_p(None), int(rows), int(pages)
+    if table.dim() != 2:
+        raise ValueError(f"table must be [rows][pages], got {tuple(table.shape)}")
+    return _dev(table, torch.int32, "table"), int(table.shape[0]), int(table.shape[1])
+
+
+def pkv_decode(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, workspace, stream=None,
+               pages=None) -> None:
+    """decode_paged; ``table=None`` with ``pages`` is decode_rows over contiguous rows."""
+    tp, rows, pages = _table(table, positions.shape[0], pages)
     _check(load_library().pkv_decode(
         pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
         _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
-        _dev(positions, torch.int32, "positions"), _dev(table, torch.int32, "table"), rows, pages,
+        _dev(positions, torch.int32, "positions"), tp, rows, pages,
         _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), _stream(stream)), "pkv_decode")
 
 
-def pkv_decode_static(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, stream=None) -> None:
+def pkv_decode_static(pool, q, k, v, q_norm_w, k_norm_w, positions, table, out, stream=None, pages=None) -> None:
     """pkv_decode without a workspace: the library's static scratch array is used instead."""
-    rows, pages = int(table.shape[0]), int(table.shape[1])
+    tp, rows, pages = _table(table, positions.shape[0], pages)
     _check(load_library().pkv_decode_static(
         pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
         _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
-        _dev(positions, torch.int32, "positions"), _dev(table, torch.int32, "table"), rows, pages,
+        _dev(positions, torch.int32, "positions"), tp, rows, pages,
         _dev(out, torch.bfloat16, "out"), _stream(stream)), "pkv_decode_static")
 
 
 def pkv_step(pool, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out, workspace,
-             stream=None) -> None:
+             stream=None, pages=None) -> None:
+    """step_paged; ``table=None`` with ``pages`` is step_packed over contiguous rows."""
     P = int(positions.shape[0])
-    rows, pages = int(table.shape[0]), int(table.shape[1])
+    tp, rows, pages = _table(table, step_positions.shape[0], pages)
     _check(load_library().pkv_step(
         pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
         _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
         _dev(positions, torch.int32, "positions"), _dev(prow, torch.int32, "prow"),
         _dev(slots, torch.int32, "slots", allow_none=True), _dev(step_positions, torch.int32, "step_positions"),
-        _dev(table, torch.int32, "table"), P, rows, pages, _dev(out, torch.bfloat16, "out"),
+        tp, P, rows, pages, _dev(out, torch.bfloat16, "out"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "pkv_step")
+
+
+def pkv_prefill(pool, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, table, out, workspace, stream=None,
+                rows=None, pages=None) -> None:
+    """prefill_paged; ``table=None`` with ``rows`` and ``pages`` is prefill over contiguous rows."""
+    P = int(positions.shape[0])
+    tp, rows, pages = _table(table, rows, pages)
+    _check(load_library().pkv_prefill(
+        pool, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
+        _dev(positions, torch.int32, "positions"), _dev(prow, torch.int32, "prow"),
+        _dev(slots, torch.int32, "slots", allow_none=True), tp, P, rows, pages,
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)), "pkv_prefill")
 
 
 def pkv_check_errors(pool, stream=None) -> int:
@@ -243,20 +272,33 @@ class PagedKVPool:
             self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.K.device)
         return self._ws
 
-    def decode(self, q, k, v, q_norm_w, k_norm_w, positions, table, out=None, stream=None) -> torch.Tensor:
+    def decode(self, q, k, v, q_norm_w, k_norm_w, positions, table, out=None, stream=None,
+               pages=None) -> torch.Tensor:
         if out is None:
             out = torch.empty_like(q)
-        ws = self.workspace(table.shape[0], table.shape[1], 0)
-        pkv_decode(self.handle, q, k, v, q_norm_w, k_norm_w, positions, table, out, ws, stream)
+        pages = table.shape[1] if table is not None else pages
+        ws = self.workspace(positions.shape[0], pages, 0)
+        pkv_decode(self.handle, q, k, v, q_norm_w, k_norm_w, positions, table, out, ws, stream, pages=pages)
         return out
 
     def step(self, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out=None,
-             stream=None) -> torch.Tensor:
+             stream=None, pages=None) -> torch.Tensor:
         if out is None:
             out = torch.empty_like(q)
-        ws = self.workspace(table.shape[0], table.shape[1], positions.shape[0])
+        pages = table.shape[1] if table is not None else pages
+        ws = self.workspace(step_positions.shape[0], pages, positions.shape[0])
         pkv_step(self.handle, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table, out, ws,
-                 stream)
+                 stream, pages=pages)
+        return out
+
+    def prefill(self, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, table, out=None, stream=None,
+                rows=None, pages=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(q)
+        pages = table.shape[1] if table is not None else pages
+        ws = self.workspace(0, pages, positions.shape[0])
+        pkv_prefill(self.handle, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, table, out, ws, stream,
+                    rows=rows, pages=pages)
         return out
 
     def check_errors(self, stream=None) -> int:

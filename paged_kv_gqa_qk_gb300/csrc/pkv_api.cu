@@ -50,15 +50,28 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
     return pl;
 }
 
-// decode: attention (which also validates rows and appends their k/v) -> combine.
-// step:   prep (validates every token, appends every k/v) -> prompt-token
-//         attention on the tensor cores -> step-row attention -> combine.
+// decode:  attention (which also validates rows and appends their k/v) -> combine.
+// step:    prep (validates every token, appends every k/v) -> prompt-token
+//          attention on the tensor cores -> step-row attention -> combine.
+// prefill: prep -> prompt-token attention.
 // All but the first kernel use programmatic dependent launch: each is
 // scheduled while the one before it drains and waits for it before touching
 // memory.
 int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
 {
     const bool decode = a.P == 0;
+    const bool timed = pool->timer_on;
+    const int slot = (int)(pool->timer_count % kTimerSlots);
+    if (!decode && a.steps == 0) {  // prompts only: prep -> prompt-token attention (the timed kernel)
+        if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+        if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
+        if (launch_prefill(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+        if (timed) {
+            if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
+            pool->timer_count++;
+        }
+        return PKV_OK;
+    }
     StepArgs as = a;  // the tokens the attention + combine kernels see
     Plan ps = plan;
     if (!decode) {
@@ -68,12 +81,10 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
         const size_t qrow = (size_t)pool->cfg.heads * pool->cfg.head_dim * 2;
         as.q = static_cast<const char*>(a.q) + (size_t)a.P * qrow;
         as.out = static_cast<char*>(a.out) + (size_t)a.P * qrow;
-        ps.tokens = a.rows;
+        ps.tokens = a.steps;
         ps.off_len += sizeof(int32_t) * a.P;
         ps.off_row += sizeof(int32_t) * a.P;
     }
-    const bool timed = pool->timer_on;
-    const int slot = (int)(pool->timer_count % kTimerSlots);
     if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
     if (launch_attn(pool, as, ps, decode, !timed, s) != cudaSuccess) return PKV_ECUDA;
     if (timed) {
@@ -225,7 +236,9 @@ static int run_step(pkv_pool* pool, const StepArgs& a, size_t ws_bytes, void* st
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
-    const Plan plan = make_plan(pool, a.P + a.rows, a.pages);
+    // contiguous rows (no table): every row's pages must be in the pool
+    if (!a.table && (int64_t)a.rows * a.pages > pool->num_pages) return PKV_ERANGE;
+    const Plan plan = make_plan(pool, a.P + a.steps, a.pages);
     if (!a.ws || ws_bytes < plan.total) return PKV_EWORKSPACE;
     return enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
 }
@@ -324,7 +337,7 @@ int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, cons
                const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows, int pages,
                void* out, void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !table || !out) return PKV_EINVAL;
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !out) return PKV_EINVAL;
     if (rows <= 0 || pages <= 0) return PKV_EINVAL;
     if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 8) || !aligned(q_norm_w, 8) ||
@@ -332,7 +345,7 @@ int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, cons
         return PKV_EINVAL;
     if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
     StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
-                  0, rows, pages, out, static_cast<char*>(workspace)};
+                  0, rows, pages, rows, out, static_cast<char*>(workspace)};
     return run_step(pool, a, workspace_bytes, stream);
 }
 
@@ -341,8 +354,7 @@ int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const 
              const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
              void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !prow || !step_positions || !table ||
-        !out)
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !prow || !step_positions || !out)
         return PKV_EINVAL;
     if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
     if ((int64_t)P + rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
@@ -352,7 +364,25 @@ int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const 
         return PKV_EINVAL;
     if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
     StepArgs a = {q, k, v, q_norm_w, k_norm_w, positions, prow, slots, step_positions, table,
-                  P, rows, pages, out, static_cast<char*>(workspace)};
+                  P, rows, pages, rows, out, static_cast<char*>(workspace)};
+    return run_step(pool, a, workspace_bytes, stream);
+}
+
+int pkv_prefill(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
+                const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
+                const int32_t* table, int P, int rows, int pages, void* out, void* workspace,
+                size_t workspace_bytes, void* stream)
+{
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !prow || !out) return PKV_EINVAL;
+    if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
+    if (P > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(q_norm_w, 8) ||
+        !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(prow, 4) || !aligned(table, 4) ||
+        (slots && !aligned(slots, 4)))
+        return PKV_EINVAL;
+    if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
+    StepArgs a = {q, k, v, q_norm_w, k_norm_w, positions, prow, slots, nullptr, table,
+                  P, rows, pages, 0, out, static_cast<char*>(workspace)};
     return run_step(pool, a, workspace_bytes, stream);
 }
 

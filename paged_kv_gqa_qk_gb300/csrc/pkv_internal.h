@@ -67,14 +67,21 @@ struct StepArgs {
     const int32_t* positions;       // [P]  (prompt tokens)
     const int32_t* prow;            // [P]
     const int32_t* slots;           // [P] or null
-    const int32_t* step_positions;  // [rows]
-    const int32_t* table;           // [rows][pages]
-    int P;
-    int rows;
-    int pages;
+    const int32_t* step_positions;  // [steps]
+    const int32_t* table;           // [rows][pages], or null: row b owns pages b*pages .. b*pages + pages - 1
+    int P;                          // prompt tokens
+    int rows;                       // table rows
+    int pages;                      // table width
+    int steps;                      // step tokens (rows for decode and step, 0 for prefill)
     void* out;
     char* ws;
 };
+
+// Pool page holding page j of table row `row` (a null table: contiguous rows).
+__device__ __forceinline__ int page_of(const int32_t* table, int pages, int row, int j)
+{
+    return table ? table[(int64_t)row * pages + j] : row * pages + j;
+}
 
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.

@@ -104,7 +104,7 @@ struct PrepParams {
     const int32_t* prow;            // [P]
     const int32_t* slots;           // [P] or null
     const int32_t* step_positions;  // [rows]
-    const int32_t* table;           // [rows][pages]
+    const int32_t* table;           // [rows][pages], or null: contiguous rows
     int P, rows, pages, num_pages, max_seq, kv_heads;
     int64_t num_slots;
     float eps;
@@ -142,11 +142,10 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
     }
     // Every page the token will read must be a pool page.
     int bad = 0;
-    const int32_t* trow = p.table + (int64_t)(row < 0 ? 0 : row) * p.pages;
     if (active && !e) {
         const int npg = pos / kPageSize + 1;
         for (int i = tid; i < npg; i += blockDim.x) {
-            const int id = trow[i];
+            const int id = page_of(p.table, p.pages, row, i);
             bad |= (id < 0 || id >= p.num_pages);
         }
     }
@@ -158,7 +157,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
             slot = p.slots[t];
             if (slot < 0 || slot >= p.num_slots) e = PKV_DEVERR_SLOT;
         } else {
-            slot = (int64_t)trow[pos / kPageSize] * kPageSize + pos % kPageSize;
+            slot = (int64_t)page_of(p.table, p.pages, row, pos / kPageSize) * kPageSize + pos % kPageSize;
         }
     }
     if (tid == 0) {
@@ -209,7 +208,7 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.tok_len = reinterpret_cast<int32_t*>(a.ws + plan.off_len);
     p.tok_row = reinterpret_cast<int32_t*>(a.ws + plan.off_row);
     p.err = pool->err;
-    prep_kernel<<<plan.tokens, 128, 0, s>>>(p);
+    prep_kernel<<<a.P + a.steps, 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -480,12 +479,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             int row, len;
             token_info(p, t, row, len);
             const int pos = len - 1;
-            const int32_t* trow = p.table + (int64_t)row * p.pages;
             bool valid = true;
             if (p.decode_mode) {  // every page the row will read must be a pool page
                 int bad = 0;
                 for (int q = lane; q < n; q += 32) {
-                    const int id = trow[q];
+                    const int id = page_of(p.table, p.pages, row, q);
                     bad |= (id < 0 || id >= p.num_pages);
                 }
                 valid = !__any_sync(kFull, bad);
@@ -505,7 +503,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                     break;
                 }
                 int page = 0;
-                if (lane == 0 && valid) page = trow[jj];
+                if (lane == 0 && valid) page = page_of(p.table, p.pages, row, jj);
                 page = __shfl_sync(kFull, page, 0);
                 if (lane == 0) {
                     const int flags = seg_flags | (s == 0 ? kFlagFirst : 0) | (s == seg - 1 ? kFlagLast : 0) |

@@ -216,10 +216,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         int i = 0;
         bool ok = true;
         for (int r = 0; r < nruns && ok; ++r) {
-            const int32_t* trow = p.table + (int64_t)sRunRow[r] * p.pages;
+            const int row = sRunRow[r];
             const int n = sRunPages[r];
             for (int b0 = 0; b0 < n && ok; b0 += 32) {
-                const int mine = (b0 + lane < n) ? trow[b0 + lane] : 0;
+                const int mine = (b0 + lane < n) ? page_of(p.table, p.pages, row, b0 + lane) : 0;
                 for (int jj = 0; jj < min(32, n - b0); ++jj, ++i) {
                     const int page = __shfl_sync(kAll, mine, jj);
                     const int st = i % kPfStages;

@@ -44,12 +44,13 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
                                  const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows,
                                  int pages, void* out, void* stream)
 {
-    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !table || !out) return PKV_EINVAL;
+    if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !out) return PKV_EINVAL;
     if (rows <= 0 || pages <= 0) return PKV_EINVAL;
     if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
     if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(out, 8) ||
         !aligned_to(q_norm_w, 8) || !aligned_to(k_norm_w, 8) || !aligned_to(positions, 4) || !aligned_to(table, 4))
         return PKV_EINVAL;
+    if (!table && (int64_t)rows * pages > pool->num_pages) return PKV_ERANGE;
     const pkv::Plan plan = pkv::make_plan(pool, rows, pages);
     if (plan.total > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERANGE;
     int dev = -1;
@@ -59,6 +60,6 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
     if (rc != PKV_OK) return rc;
 
     const pkv::StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
-                             0, rows, pages, out, static_cast<char*>(scratch)};
+                             0, rows, pages, rows, out, static_cast<char*>(scratch)};
     return pkv::enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
 }

@@ -21,14 +21,22 @@ def run_gpu(wl: W.Workload, ctas: int = 0, explicit_slots=None, table=None, step
         pkv.pkv_set_ctas(pool.handle, ctas)
     q, k, v, qw, kw = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w))
     tab = (wl.table if table is None else torch.as_tensor(table)).to(dev)
+    pages = int(tab.shape[1])
+    if wl.contiguous and table is None:
+        tab = None   # the library's own contiguous-row layout
     sp = (wl.step_positions if step_positions is None else torch.as_tensor(step_positions)).to(dev)
     for _ in range(repeat):
         if wl.kind == "decode":
-            out = pool.decode(q, k, v, qw, kw, sp, tab)
+            out = pool.decode(q, k, v, qw, kw, sp, tab, pages=pages)
         else:
             pos = (wl.positions if positions is None else torch.as_tensor(positions)).to(dev)
             slots = None if explicit_slots is None else torch.as_tensor(explicit_slots, dtype=torch.int32).to(dev)
-            out = pool.step(q, k, v, qw, kw, pos, wl.prow.to(dev), slots, sp, tab)
+            if wl.kind == "step":
+                out = pool.step(q, k, v, qw, kw, pos, wl.prow.to(dev), slots, sp, tab, pages=pages)
+            else:
+                P = wl.P
+                out = pool.prefill(q[:P], k[:P], v[:P], qw, kw, pos, wl.prow.to(dev), slots, tab,
+                                   rows=wl.R, pages=pages)
     flags = pool.check_errors()
     res = (out.cpu(), K.cpu(), V.cpu(), flags)
     pool.close()
@@ -45,6 +53,8 @@ def run_oracle(wl: W.Workload, sel=None, table=None, step_positions=None, positi
     else:
         pos = (wl.positions if positions is None else torch.as_tensor(positions)).numpy()
         out, err = oracle.step(K, V, *args, pos, wl.prow.numpy(), None, sp, tab, cfg=wl.cfg, sel=sel)
+        if wl.kind == "prefill":   # the table rows take no step: prompt outputs only
+            out = out[:wl.P]
     return out, K, V, err
 
 

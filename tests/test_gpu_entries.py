@@ -1,0 +1,114 @@
+"""GPU parity of the prompt-only entry (pkv_prefill, the pages' prefill_paged)
+and of the contiguous-row layout (a NULL table: decode_rows, prefill_packed,
+step_packed) against the fp64 oracle, with the same bar as the other parity
+tests.  The oracle sees the layout as its identity page table."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_qk_gb300 as pkv
+import workloads as W
+from _harness import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ prefill_paged
+
+def test_prefill_chunks_over_prefilled_pages():
+    """Four prompts, ragged, three of them continuing a row at a position
+    inside a page (chunked prefill over keys the row already holds)."""
+    wl = W.make_prefill("prefill chunks", [70, 5, 130, 300], [60, 0, 500, 64], seed=31, table_pages=14)
+    ref = run_oracle(wl)
+    assert ref[3] == 0
+    compare(wl, run_gpu(wl), ref, label="prefill derived slots")
+    slots = oracle.page_slots(wl.table.numpy(), wl.prow.numpy(), wl.positions.numpy())
+    compare(wl, run_gpu(wl, explicit_slots=slots), ref, label="prefill explicit slots")
+    compare(wl, run_gpu(wl, repeat=2), ref, label="prefill x2")
+
+
+def test_prefill_shared_prefix_pages():
+    """Two prompts whose rows list the same first pages (a shared prefix that
+    neither writes) and continue past it on pages of their own."""
+    wl = W.make_prefill("prefill shared prefix", [100, 33], [128, 128], seed=32, table_pages=5)
+    table = wl.table.clone()
+    table[1, :2] = table[0, :2]          # row 1 reads row 0's two prefix pages
+    ref = run_oracle(wl, table=table)
+    assert ref[3] == 0
+    compare(wl, run_gpu(wl, table=table), ref, label="prefill shared prefix")
+
+
+def test_prefill_2048_tokens_sampled():
+    """The step mix's prompt side alone: 4 prompts, P = 2048 (each >= 64),
+    continuing at U[0, 4096]; every 16th token and each prompt's ends."""
+    wl = W.prefill_mix()
+    P = wl.P
+    ends = np.cumsum([0] + wl.meta["prompt_lengths"])
+    sel = sorted(set(range(0, P, 16)) | set(ends[:-1].tolist()) | set((ends[1:] - 1).tolist()))
+    compare(wl, run_gpu(wl), run_oracle(wl, sel=sel), sel=sel, label="prefill P=2048")
+
+
+def test_prefill_invalid_tokens():
+    wl = W.make_prefill("prefill errors", [40, 30, 20], [0, 100, 5], seed=33, table_pages=4)
+    pos = wl.positions.clone()
+    pos[3] = 40960                       # beyond max_seq
+    pos[45] = 4 * 64                     # beyond the table width
+    table = wl.table.clone()
+    table[2, 0] = wl.num_pages + 3       # not a pool page: all of prompt 2 is skipped
+    gpu = run_gpu(wl, table=table, positions=pos)
+    ref = run_oracle(wl, table=table, positions=pos)
+    assert ref[3] == (oracle.ERR_POSITION | oracle.ERR_PAGE)
+    compare(wl, gpu, ref, label="prefill errors")
+    assert not gpu[0][3].float().abs().sum() and not gpu[0][45].float().abs().sum()
+    assert not gpu[0][70:].float().abs().sum()
+
+
+# ------------------------------------------------------------------ contiguous rows (NULL table)
+
+@pytest.mark.parametrize("ctas", [0, 7])
+def test_decode_rows_contiguous(ctas):
+    """decode_rows: 64 rows of 640 positions each (10 pages a row), lengths
+    U[1, 640]; the rows own their pages in pool order."""
+    wl = W.make_decode("decode_rows 64 x 640", (64, 1, 640), seed=34, table_pages=10, contiguous=True)
+    assert wl.contiguous and wl.num_pages == 640
+    compare(wl, run_gpu(wl, ctas=ctas), run_oracle(wl), label=f"decode_rows ctas={ctas}")
+
+
+def test_prefill_packed_contiguous():
+    """prefill_packed: prompts each filling its own row from position 0."""
+    wl = W.make_prefill("prefill_packed", [1, 64, 65, 200, 127], [0] * 5, seed=36, table_pages=4, contiguous=True)
+    compare(wl, run_gpu(wl), run_oracle(wl), label="prefill_packed")
+
+
+def test_step_packed_contiguous():
+    """step_packed: prompts continuing their rows plus decode rows, all contiguous."""
+    wl = W.make_step("step_packed", prompt_lengths=[70, 5, 130], prompt_starts=[0, 60, 100],
+                     decode_lengths=[90, 3, 64, 65, 1, 640], seed=37, table_pages=10, contiguous=True)
+    ref = run_oracle(wl)
+    compare(wl, run_gpu(wl), ref, label="step_packed")
+    compare(wl, run_gpu(wl, ctas=5), ref, label="step_packed ctas=5")
+
+
+def test_contiguous_rows_must_fit_the_pool():
+    """rows * pages beyond the pool is a host error, with nothing enqueued."""
+    wl = W.make_decode("too wide", [10, 20], seed=38, table_pages=2, contiguous=True)
+    dev = torch.device("cuda")
+    K, V = wl.K0.to(dev), wl.V0.to(dev)
+    pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+    q, k, v, qw, kw, sp = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w, wl.step_positions))
+    out = torch.zeros_like(q)
+    ws = pool.workspace(2, 3, 0)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_decode(pool.handle, q, k, v, qw, kw, sp, None, out, ws, pages=3)
+    assert ei.value.code == pkv.PKV_ERANGE
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_prefill(pool.handle, q[:1], k[:1], v[:1], qw, kw, pos, pos, None, None, out[:1],
+                        pool.workspace(0, 3, 1), rows=2, pages=3)
+    assert ei.value.code == pkv.PKV_ERANGE
+    torch.cuda.synchronize()
+    assert not out.any()
+    assert torch.equal(K.cpu(), wl.K0) and torch.equal(V.cpu(), wl.V0)
+    assert pool.check_errors() == 0
+    pool.close()

@@ -304,6 +304,40 @@ def test_brute_force_tiny_shapes():
         np.testing.assert_allclose(out[0, h], o, rtol=1e-13, atol=1e-15)
 
 
+# ------------------------------------------------------------------ contiguous rows: prefill_packed, decode_rows
+
+def test_prefill_over_contiguous_rows_equals_packed_attention():
+    """Prompts that each fill their own row from position 0, over the
+    contiguous-row layout (identity table), give prefill_packed's result: each
+    token attends to its own prompt's tokens up to itself (mask segments equal
+    and positions[j] <= positions[i]), computed here from the pass's own
+    normed and roped keys with torch SDPA; and token p lands at slot
+    prow[p] * pages * page_size + positions[p]."""
+    wl = W.make_prefill("packed", [3, 70, 1, 64], [0, 0, 0, 0], seed=41, table_pages=2, contiguous=True)
+    assert wl.kind == "prefill" and wl.contiguous
+    S, G, H = CFG["page_size"], CFG["kv_heads"], CFG["heads"]
+    q, k, v, qw, kw = (W.bits(t) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w))
+    pos, prow = wl.positions.numpy(), wl.prow.numpy()
+    K, V = W.bits(wl.K0).copy(), W.bits(wl.V0).copy()
+    out, err = oracle.step(K, V, q, k, v, qw, kw, pos, prow, None, wl.step_positions.numpy(), wl.table.numpy())
+    assert err == 0
+    P = wl.P
+    khat = np.stack([np.stack([oracle.round_bf16(complex_rope(torch_norm(k[t, g], kw), int(pos[t])))
+                               for g in range(G)]) for t in range(P)])        # [P][G][D] bf16 bits
+    for t in range(P):
+        slot = int(prow[t]) * wl.pages * S + int(pos[t])
+        for g in range(G):
+            np.testing.assert_array_equal(K[g, slot], khat[t, g])
+            np.testing.assert_array_equal(V[g, slot], v[t, g])
+    for i in range(P):
+        own = [j for j in range(P) if prow[j] == prow[i] and pos[j] <= pos[i]]
+        qh = np.stack([complex_rope(torch_norm(q[i, h], qw), int(pos[i])) for h in range(H)])
+        Kc = oracle.bf16_to_f64(khat[own].transpose(1, 0, 2))
+        Vc = oracle.bf16_to_f64(v[own].transpose(1, 0, 2))
+        np.testing.assert_allclose(out[i], sdpa_f64(qh, Kc, Vc), rtol=1e-10, atol=1e-12)
+    assert not out[P:].any()   # the table rows take no step
+
+
 # ------------------------------------------------------------------ a7 prefill chunk == sequential decode
 
 def test_step_prefill_equals_sequential_decode():

@@ -67,7 +67,13 @@ class Workload:
 
     @property
     def kind(self) -> str:
-        return "decode" if self.positions is None else "step"
+        """"decode", "step" or "prefill" (prompt tokens only; the table rows take no step)."""
+        return self.meta.get("mode") or ("decode" if self.positions is None else "step")
+
+    @property
+    def contiguous(self) -> bool:
+        """True when ``table`` is the contiguous-row identity (row b owns pages b*pages ..)."""
+        return bool(self.meta.get("contiguous"))
 
 
 def bits(t: torch.Tensor):
@@ -104,14 +110,34 @@ def _tokens(gen: torch.Generator, cfg: dict, n: int):
     return q, k, v, qw, kw
 
 
+def contiguous_table(rows: int, pages: int) -> torch.Tensor:
+    """The contiguous-row layout as a page table: row b owns pool pages b*pages .. b*pages+pages-1."""
+    return torch.arange(rows * pages, dtype=torch.int32).view(rows, pages)
+
+
 def make_decode(name: str, lengths, seed: int, cfg: dict | None = None, table_pages: int | None = None,
-                share_groups: int = 0, share_range=(8, 32), scratch: bool = True) -> Workload:
+                share_groups: int = 0, share_range=(8, 32), scratch: bool = True,
+                contiguous: bool = False) -> Workload:
     """A decode_paged workload: one step token per row, row b at position lengths[b]-1.
 
     share_groups > 0: consecutive groups of that many rows share their first
     s_g pages, s_g = min(U{share_range}, smallest write-page index in the
     group), so shared pages are full pages strictly before every write.
+    contiguous: the decode_rows layout, row b owning table_pages pages of its
+    own in pool order (pool of rows * table_pages pages, table the identity).
     """
+    if contiguous:
+        assert not share_groups and table_pages is not None
+        wl = make_decode(name, lengths, seed, cfg, table_pages, scratch=False)
+        R, S = wl.R, wl.cfg["page_size"]
+        gen = torch.Generator().manual_seed(seed + 1)
+        G, D = wl.cfg["kv_heads"], wl.cfg["head_dim"]
+        num_pages = R * table_pages
+        K0 = _randn_bf16(gen, (G, num_pages * S, D))
+        V0 = _randn_bf16(gen, (G, num_pages * S, D))
+        meta = dict(wl.meta, contiguous=True)
+        return Workload(name, wl.cfg, num_pages, K0, V0, wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w,
+                        contiguous_table(R, table_pages), wl.step_positions, meta=meta)
     cfg = dict(DEFAULT_CONFIG, **(cfg or {}))
     S = cfg["page_size"]
     gen = torch.Generator().manual_seed(seed)
@@ -173,13 +199,15 @@ def make_decode(name: str, lengths, seed: int, cfg: dict | None = None, table_pa
 
 
 def make_step(name: str, prompt_lengths, prompt_starts, decode_lengths, seed: int, cfg: dict | None = None,
-              table_pages: int | None = None, gen: torch.Generator | None = None) -> Workload:
+              table_pages: int | None = None, gen: torch.Generator | None = None,
+              contiguous: bool = False) -> Workload:
     """A step_paged workload: prompt chunks packed end to end, then one step per decode row.
 
     Table rows 0..R_d-1 are the decode rows; rows R_d..R_d+M-1 hold the M
     prompts (they take no step: step_positions -1).  Prompt j continues at
     position prompt_starts[j] over pre-filled pages and spans
-    prompt_lengths[j] tokens.
+    prompt_lengths[j] tokens.  contiguous: the step_packed layout (identity
+    table, pool of rows * table_pages pages).
     """
     cfg = dict(DEFAULT_CONFIG, **(cfg or {}))
     S = cfg["page_size"]
@@ -191,12 +219,16 @@ def make_step(name: str, prompt_lengths, prompt_starts, decode_lengths, seed: in
     npages = [_pages_for(x, S) for x in row_len]
     width = table_pages if table_pages is not None else max(npages)
     assert width >= max(npages)
-    num_pages = sum(npages) + 1
-    perm = (torch.randperm(num_pages - 1, generator=gen) + 1).tolist()
-    table = torch.zeros(R, width, dtype=torch.int32)
-    it = iter(perm)
-    for b in range(R):
-        table[b, :npages[b]] = torch.tensor([next(it) for _ in range(npages[b])], dtype=torch.int32)
+    if contiguous:
+        num_pages = R * width
+        table = contiguous_table(R, width)
+    else:
+        num_pages = sum(npages) + 1
+        perm = (torch.randperm(num_pages - 1, generator=gen) + 1).tolist()
+        table = torch.zeros(R, width, dtype=torch.int32)
+        it = iter(perm)
+        for b in range(R):
+            table[b, :npages[b]] = torch.tensor([next(it) for _ in range(npages[b])], dtype=torch.int32)
     positions, prow = [], []
     for j in range(M):
         positions += list(range(int(prompt_starts[j]), int(prompt_starts[j]) + int(prompt_lengths[j])))
@@ -211,10 +243,27 @@ def make_step(name: str, prompt_lengths, prompt_starts, decode_lengths, seed: in
     meta = dict(decode_lengths=[int(x) for x in decode_lengths], prompt_lengths=[int(x) for x in prompt_lengths],
                 prompt_starts=[int(x) for x in prompt_starts],
                 logical_kv_bytes=bpp * sum(int(x) for x in decode_lengths),
-                prefill_attended_positions=sum(p + 1 for p in positions), seed=seed)
+                prefill_attended_positions=sum(p + 1 for p in positions), seed=seed, contiguous=contiguous)
     return Workload(name, cfg, num_pages, K0, V0, q, k, v, qw, kw, table, step_positions,
                     positions=torch.tensor(positions, dtype=torch.int32),
                     prow=torch.tensor(prow, dtype=torch.int32), meta=meta)
+
+
+def make_prefill(name: str, prompt_lengths, prompt_starts, seed: int, cfg: dict | None = None,
+                 table_pages: int | None = None, gen: torch.Generator | None = None,
+                 contiguous: bool = False) -> Workload:
+    """A prefill_paged workload: make_step's prompts with no decode rows.
+
+    Its M table rows all take no step, so q/k/v keep M unused step tokens
+    after the P prompt tokens (the oracle's step form); a prefill call takes
+    the first P.
+    """
+    wl = make_step(name, prompt_lengths, prompt_starts, [], seed, cfg, table_pages, gen, contiguous)
+    wl.meta["mode"] = "prefill"
+    # K/V the prompts' attention reads: each prompt's row up to its last position
+    wl.meta["logical_kv_bytes"] = kv_bytes_per_position(wl.cfg) * sum(
+        int(s) + int(n) for s, n in zip(prompt_starts, prompt_lengths))
+    return wl
 
 
 # ------------------------------------------------------------------ the five configs
@@ -253,18 +302,37 @@ def config4() -> Workload:
                        (256, 1024, 8192), seed=1004, table_pages=128, share_groups=16)
 
 
+def _prompt_mix(gen: torch.Generator, M: int = 4, P: int = 2048, minlen: int = 64, start_hi: int = 4096):
+    """M prompt lengths summing to P (each >= minlen) and their start positions U[0, start_hi]."""
+    cuts = sorted(_uniform_int(gen, 0, P - M * minlen, M - 1).tolist())
+    bounds = [0] + cuts + [P - M * minlen]
+    plen = [minlen + bounds[j + 1] - bounds[j] for j in range(M)]
+    starts = _uniform_int(gen, 0, start_hi, M).tolist()
+    return plen, starts
+
+
 def config5() -> Workload:
     """step_paged: 4 prompts totalling P=2048 (each >= 64) continuing at U[0,4096], plus 128 rows x U[1024,8192]."""
     seed = 1005
     gen = torch.Generator().manual_seed(seed)
-    M, P, minlen = 4, 2048, 64
-    cuts = sorted(_uniform_int(gen, 0, P - M * minlen, M - 1).tolist())
-    bounds = [0] + cuts + [P - M * minlen]
-    plen = [minlen + bounds[j + 1] - bounds[j] for j in range(M)]
-    starts = _uniform_int(gen, 0, 4096, M).tolist()
+    plen, starts = _prompt_mix(gen)
     dlen = _uniform_int(gen, 1024, 8192, 128).tolist()
     return make_step("step: 4 prompts P=2048 at U[0,4096] + 128 decode rows x U[1024,8192]",
                      plen, starts, dlen, seed=seed, table_pages=128, gen=gen)
+
+
+def prefill_mix(seed: int = 1006) -> Workload:
+    """prefill_paged: config5's kind of prompt side alone, 4 prompts P=2048 continuing at U[0,4096]."""
+    gen = torch.Generator().manual_seed(seed)
+    plen, starts = _prompt_mix(gen)
+    return make_prefill("prefill: 4 prompts P=2048 at U[0,4096]", plen, starts, seed=seed, table_pages=128,
+                        gen=gen)
+
+
+def rows_mix(seed: int = 1007) -> Workload:
+    """decode_rows: 64 contiguous rows of 640 positions (10 pages each), lengths U[1, 640]."""
+    return make_decode("decode_rows 64 rows x U[1,640], 640 positions a row", (64, 1, 640), seed=seed,
+                       table_pages=10, contiguous=True)
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
