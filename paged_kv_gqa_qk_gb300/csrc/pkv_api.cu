@@ -46,6 +46,8 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
     off = align_up(off + sizeof(float) * slots * kGroup * kHeadDim, 256);
     pl.off_plse = off;
     off = align_up(off + sizeof(float) * slots * kGroup, 256);
+    pl.off_sched = off;
+    off = align_up(off + sizeof(int32_t), 256);
     pl.total = off;
     return pl;
 }

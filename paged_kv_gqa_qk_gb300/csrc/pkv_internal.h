@@ -52,7 +52,9 @@ struct Plan {
     int tokens;         // P + rows
     int pages;          // table width
     int ctas;           // attention grid size C
-    size_t off_len, off_row, off_prefix, off_unit_ok, off_po, off_plse, total;
+    size_t off_len, off_row, off_prefix, off_unit_ok, off_po, off_plse;
+    size_t off_sched;   // prompt attention: counter of claimed work units (zeroed by prep_kernel)
+    size_t total;
 };
 
 Plan make_plan(const pkv_pool* pool, int tokens, int pages);

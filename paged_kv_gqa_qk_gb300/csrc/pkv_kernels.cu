@@ -114,6 +114,7 @@ struct PrepParams {
     __nv_bfloat16* V;
     int32_t* tok_len;               // [tokens]  attended length, 0 = skip
     int32_t* tok_row;               // [tokens]  table row
+    int32_t* sched;                 // work-unit counter of the prompt attention, zeroed here
     uint32_t* err;
 };
 
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
         }
     }
     if (tid == 0) {
+        if (t == 0) *p.sched = 0;
         const bool ok = active && !e;
         p.tok_len[t] = ok ? pos + 1 : 0;
         p.tok_row[t] = ok ? row : 0;
@@ -207,6 +209,7 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.V = static_cast<__nv_bfloat16*>(pool->v);
     p.tok_len = reinterpret_cast<int32_t*>(a.ws + plan.off_len);
     p.tok_row = reinterpret_cast<int32_t*>(a.ws + plan.off_row);
+    p.sched = reinterpret_cast<int32_t*>(a.ws + plan.off_sched);
     p.err = pool->err;
     prep_kernel<<<a.P + a.steps, 128, 0, s>>>(p);
     return cudaGetLastError();

@@ -1,31 +1,42 @@
-// Prompt-chunk attention of step_paged on tcgen05 tensor cores (sm_103a).
+// Prompt-chunk attention of step_paged / prefill_paged on tcgen05 tensor
+// cores (sm_103a).
 //
 // qwen3-8b Nest files, src/attention.linnet, GroupedQueryAttention.step_paged
-// (and prefill_paged): after every token of the call has been written to the
+// and prefill_paged: after every token of the call has been written to the
 // pool (prep_kernel), prompt token p attends over table[rows[p]] for
 // positions 0..positions[p] -- its own chunk's earlier keys included.
 //
-// A CTA takes a tile of 32 consecutive prompt tokens and one kv head g.  The
-// 4 query heads of g times the 32 tokens are the M = 128 rows of the matrix
-// products, row m = head (m / 32) of the group, token (m % 32) of the tile, so
-// tensor-memory lane m belongs to thread m of the four softmax warps.  For
-// every page j of the row (up to the tile's last position):
-//   S_j  = Q K_j^T           128 x 64,  K = 128 dims   (tcgen05, into TMEM)
-//   P_j  = 2^(S_j - m)       causal mask, online max m (softmax warps, bf16 to smem)
-//   O   += P_j V_j           128 x 128, K = 64 positions (tcgen05, into TMEM)
+// Work unit: a tile of 64 consecutive prompt tokens and one kv head g.  The
+// tile is two halves of 32 tokens, one per softmax group; in each half the 4
+// query heads of g times the 32 tokens are the M = 128 rows of the products,
+// row m = head (m / 32) of the group, token (m % 32) of the half, so
+// tensor-memory lane m belongs to thread m of the group's four warps.  Both
+// halves read the same blocks of two pages (128 keys) of the row; per block b:
+//   S_h  = Q_h K_b^T         128 x 128, K = 128 dims   (tcgen05, into TMEM)
+//   P_h  = 2^(S_h - m_h)     causal mask, online max   (softmax group h, bf16
+//                            back into TMEM over the first half of S_h)
+//   O_h += P_h V_b           128 x 128, K = 128 keys   (tcgen05, A from TMEM)
 // Q carries the QK-norm, the RoPE and the score scale log2(e)/sqrt(128), so S
-// is in base-2 units.  The running max is only moved (and O, l rescaled in
-// place) when a page raises it by more than 8: in between, P stays below 2^8.
+// is in base-2 units.  The running max only moves (and O, l are rescaled in
+// place) when a block raises it by more than 8: in between, P stays below 2^8.
 //
-// Warp roles: 0-3 softmax (and the q preparation and the epilogue), 4 TMA
-// producer (pages of K and V through a 3-stage ring, the layout the decode
-// kernel also uses), 5 tensor-memory allocation and the MMA-issuing thread.
-// S is double-buffered in tensor memory and P in shared memory, so the
-// products of page j+1 overlap the softmax of page j.
+// The two groups ping-pong: the tensor cores run one group's products while
+// the other group's softmax runs.  The issuing order per block is
+//   PV_0(b), S_0(b+1), PV_1(b), S_1(b+1)
+// so that S_h(b+1), which overwrites P_h(b) in tensor memory, is issued after
+// the product that reads it (tcgen05 operations of one thread run in order).
 //
-// A tile whose tokens belong to several table rows (where one prompt ends and
-// the next begins) is processed once per row; tokens of the other rows are
-// masked out of that pass.
+// Warp roles: 0-3 softmax group 0, 4-7 softmax group 1 (each also builds its
+// Q half and writes its outputs), 8 TMA producer (the K and the V of each
+// block through a ring of four 32 KiB stages), 9 tensor-memory allocation and
+// the MMA-issuing thread.
+//
+// The grid is persistent, one CTA per SM.  Units are taken from a counter in
+// the workspace in decreasing order of the tile's page count (longest first),
+// an order every CTA derives identically from the token table.  A tile whose
+// tokens belong to several table rows (where one prompt ends and the next
+// begins) is processed once per row; tokens of the other rows are masked out
+// of that pass.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -37,30 +48,47 @@ namespace pkv {
 namespace {
 
 constexpr uint32_t kAll = 0xffffffffu;
-constexpr int kTileTok = 32;                 // prompt tokens per tile
-constexpr int kTileRows = kTileTok * kGroup;  // 128 = M
-constexpr int kPfStages = 3;
-constexpr int kPfStageBytes = 4 * 8192;      // K lo, K hi, V lo, V hi (one page, one kv head)
-constexpr int kPfThreads = 6 * 32;
-constexpr int kSoftmaxWarps = 4, kProducer = 4, kIssuer = 5;
-constexpr uint32_t kTmemCols = 256;          // S buffers at columns 0 and 64, O at 128..255
-constexpr float kRescale = 8.f;              // log2 headroom before the running max moves
+constexpr int kHalfTok = 32;                   // tokens of one half (one softmax group)
+constexpr int kTileTok = 2 * kHalfTok;         // tokens of a tile
+constexpr int kRowsM = kHalfTok * kGroup;      // 128 = M of every product
+constexpr int kBlockKeys = 2 * kPageSize;      // keys of a block: two pages
+constexpr int kPfStages = 4;                   // ring stages, each the K or the V of one block
+constexpr int kPfStageBytes = kBlockKeys * kHeadDim * 2;  // 32 KiB
+constexpr int kHalfBytes = kPfStageBytes / 2;  // one 64-dim half of a stage: [2 pages][64 keys][128 B]
+constexpr int kGroups = 2;
+constexpr int kProducer = 4 * kGroups, kIssuer = kProducer + 1;
+constexpr int kPfThreads = 32 * 4 * (kGroups + 1);  // three warpgroups; warps 10 and 11 only take part in barriers
+// Registers per thread: the launch gives every thread kRegsLaunch; the third
+// warpgroup (producer, issuer) hands registers to the two softmax groups.
+constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 224, kRegsOther = 56;
+static_assert(kGroups * 128 * kRegsSoftmax + 128 * kRegsOther <= kPfThreads * kRegsLaunch, "register split");
+static_assert(kRegsLaunch * kPfThreads <= 65536, "register file");
+constexpr uint32_t kTmemCols = 512;            // group h: S/P at 256h, O at 256h + 128
+constexpr float kRescale = 8.f;                // log2 headroom before the running max moves
+constexpr int kMaxSortTiles = 2048;            // larger calls take tiles in token order
+constexpr int kSortIdxBits = 11;
 
 struct PfSmem {
-    static constexpr int kQ = 0;                                  // bf16 [2 halves][128 rows][128 B], swizzled
-    static constexpr int kRing = kQ + 2 * kTileRows * 128;        // stages x 32 KiB
-    static constexpr int kP = kRing + kPfStages * kPfStageBytes;  // bf16 [2 buffers][128 rows][128 B]
-    static constexpr int kTok = kP + 2 * kTileRows * 128;         // int pos[32], row[32]
-    static constexpr int kRuns = kTok + 2 * kTileTok * 4;         // int row[32], npages[32], count
-    static constexpr int kW = kRuns + (2 * kTileTok + 4) * 4;     // bf16 q_norm weights [128]
+    static constexpr int kQ = 0;                                    // 2 groups x [2 halves][128 rows][128 B]
+    static constexpr int kRing = kQ + kGroups * 2 * kRowsM * 128;   // stages x 32 KiB
+    static constexpr int kSort = kRing + kPfStages * kPfStageBytes;  // uint32 [kMaxSortTiles]
+    static constexpr int kTok = kSort + 4 * kMaxSortTiles;          // int pos[64], row[64]
+    static constexpr int kRuns = kTok + 2 * kTileTok * 4;           // int row[64], npages[64], count, unit
+    static constexpr int kW = kRuns + (2 * kTileTok + 4) * 4;       // bf16 q_norm weights [128]
     static constexpr int kBars = kW + 256;
-    // full[S], empty[S], s_ready[2], p_ready[2], o_done[2], epi_done
-    static constexpr int kNumBars = 2 * kPfStages + 7;
+    // full[S], empty[S], s_ready[2], p_ready[2], o_done[2], epi[2], drain
+    static constexpr int kNumBars = 2 * kPfStages + 4 * kGroups + 1;
+    // at a unit's start the ring holds the tile's q rows and RoPE rows for the Q preparation
+    static constexpr int kStageQ = kRing;                           // [64 tokens][4 heads][128] bf16
+    static constexpr int kStageRope = kRing + kTileTok * kGroup * kHeadDim * 2;  // [64 tokens][64] float2
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 16;
     static constexpr int kBytes = kFlag + 16;
     static constexpr int kAlloc = kBytes + 1024;
 };
+static_assert(PfSmem::kAlloc <= 227 * 1024, "prefill shared memory");
+static_assert(PfSmem::kStageRope + kTileTok * kRopeHalf * 8 <= PfSmem::kRing + kPfStages * kPfStageBytes,
+              "staging fits the ring");
 
 // byte offset of element c (< 64) of row r in a [rows][64 bf16] tile with 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2; }
@@ -70,308 +98,442 @@ struct PfParams {
     const __nv_bfloat16* qw;  // q_norm weights [128]
     const int32_t* tok_len;   // [P] attended length from prep_kernel, 0 = skip
     const int32_t* tok_row;   // [P]
-    const int32_t* table;     // [rows][pages]
+    const int32_t* table;     // [rows][pages], or null (contiguous rows)
     const float2* rope_hi;    // (cos, sin) [max_seq][64]
     __nv_bfloat16* out;       // [P + rows][heads][128]
+    int32_t* sched;           // unit counter, zero at launch
     uint32_t* err;
     int P, pages, heads, kv_heads, ntiles;
     float eps;
 };
 
-__global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, PfParams p)
+
+// Shared-memory addresses and launch-wide values every role needs.
+struct PfCtx {
+    uint32_t base;   // 1024-aligned shared address of the layout
+    uint8_t* sbase;  // the same, generic
+    uint32_t bar_full, bar_empty, bar_s, bar_p, bar_o, bar_epi, bar_drain;
+    uint32_t tmem;
+    int* sPos;
+    int* sRow;
+    int* sRunRow;
+    int* sRunPages;
+    int* sNumRuns;
+    int* sUnit;
+    const uint32_t* sKey;
+    volatile int* abort_flag;
+    int nunits;
+    bool sorted;
+};
+
+__device__ __forceinline__ int tile_of(const PfCtx& c, const PfParams& p, int u)
 {
-    using L = PfSmem;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_base = smem_u32(smem_raw);
-    const uint32_t base = (raw_base + 1023u) & ~1023u;
-    uint8_t* sbase = smem_raw + (base - raw_base);
-    const uint32_t bar0 = base + L::kBars;
-    const uint32_t bar_full = bar0, bar_empty = bar0 + 8 * kPfStages;
-    const uint32_t bar_s = bar0 + 16 * kPfStages, bar_p = bar_s + 16, bar_o = bar_p + 16, bar_epi = bar_o + 16;
-    int* sPos = reinterpret_cast<int*>(sbase + L::kTok);
-    int* sRow = sPos + kTileTok;
-    int* sRunRow = reinterpret_cast<int*>(sbase + L::kRuns);
-    int* sRunPages = sRunRow + kTileTok;
-    int* sNumRuns = sRunPages + kTileTok;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kFlag);
+    return c.sorted ? (kMaxSortTiles - 1) - (int)(c.sKey[u / p.kv_heads] & ((1u << kSortIdxBits) - 1))
+                    : u / p.kv_heads;
+}
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tile = blockIdx.x % p.ntiles, g = blockIdx.x / p.ntiles;
-    const int p0 = tile * kTileTok;
+// S_h = Q_h K^T for the block of npg pages in the ring stage at `kst`, into
+// group h's S columns; its completion arrives on s_ready[h].  A descriptor of
+// k-step k is the k = 0 one plus the step's byte offset / 16 (no carry: shared
+// addresses stay below 2^18).
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t qb, uint32_t kst, uint32_t bar_s, int h, int npg)
+{
+    constexpr uint32_t id_s128 = umma_idesc_bf16(kRowsM, kBlockKeys, 0, 0);
+    constexpr uint32_t id_s64 = umma_idesc_bf16(kRowsM, kPageSize, 0, 0);
+    const uint32_t id = npg == 2 ? id_s128 : id_s64;
+    const uint64_t a0 = umma_desc_sw128(qb + h * (2 * kRowsM * 128), 16, 1024);
+    const uint64_t b0 = umma_desc_sw128(kst, 16, 1024);
+    const uint32_t d = tmem + 256 * h;
+    umma_bf16(d, a0, b0, id, false);
+#pragma unroll
+    for (int k = 1; k < kHeadDim / 16; ++k) {
+        const uint32_t ao = ((k >> 2) * (kRowsM * 128) + (k & 3) * 32) >> 4;
+        const uint32_t bo = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
+        umma_bf16_acc(d, a0 + ao, b0 + bo, id);
+    }
+    umma_commit(bar_s + 8 * h);
+}
 
-    if (tid == 0) {
-        for (int i = 0; i < 2 * kPfStages; ++i) mbar_init(bar0 + 8 * i, 1);  // full (producer), empty (commit)
-        mbar_init(bar_s, 1);
-        mbar_init(bar_s + 8, 1);
-        mbar_init(bar_p, kSoftmaxWarps);
-        mbar_init(bar_p + 8, kSoftmaxWarps);
-        mbar_init(bar_o, 1);
-        mbar_init(bar_o + 8, 1);
-        mbar_init(bar_epi, kSoftmaxWarps);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == kIssuer) tmem_alloc(base + L::kTmemSlot, kTmemCols);
-    if (warp == kProducer && lane == 0) {
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-    }
-    pdl_wait();  // prep_kernel's appends and token table
+// O_h (+)= P_h V for the npg pages of the V stage at `vs`; the first product
+// of a run's first block overwrites O_h.
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t vs, int h, int npg, bool accumulate)
+{
+    constexpr uint32_t id_pv = umma_idesc_bf16(kRowsM, kHeadDim, 0, 1);
+    const uint64_t b0 = umma_desc_sw128(vs, kHalfBytes, 1024);
+    const uint32_t d = tmem + 256 * h + 128, a = tmem + 256 * h;
+    umma_bf16_ts(d, a, b0, id_pv, accumulate);
+#pragma unroll
+    for (int k = 1; k < kBlockKeys / 16; ++k)
+        if (k < npg * (kPageSize / 16)) umma_bf16_ts_acc(d, a + 8 * k, b0 + ((k * 2048) >> 4), id_pv);
+}
 
-    // ---- the tile's tokens, and its runs (one per table row among its valid tokens)
-    if (tid < kTileTok) {
-        const int t = p0 + tid;
-        const int len = t < p.P ? p.tok_len[t] : 0;
-        sPos[tid] = len - 1;  // -1: not a token, or skipped
-        sRow[tid] = len > 0 ? p.tok_row[t] : -1;
-    } else if (tid < 2 * kTileTok) {
-        reinterpret_cast<uint2*>(sbase + L::kW)[tid - kTileTok] = reinterpret_cast<const uint2*>(p.qw)[tid - kTileTok];
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int nr = 0;
-        for (int i = 0; i < kTileTok; ++i) {
-            if (sPos[i] < 0) continue;
-            int r = 0;
-            while (r < nr && sRunRow[r] != sRow[i]) ++r;
-            if (r == nr) {
-                sRunRow[nr] = sRow[i];
-                sRunPages[nr] = 0;
+// Every role runs its own unit loop through the same four CTA barriers per
+// unit: (1) the unit the producer claimed is visible, (2) the tile's tokens
+// are loaded, (3) its runs and Q are ready, (4) every product of the unit has
+// completed (the epilogues waited for the last one), so that the next unit may
+// rewrite Q and the token table.
+
+// ---------------------------------------------------------------- producer (warp 8)
+__device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, int lane)
+{
+    int q_load = 0;  // ring loads so far, across units
+    const uint64_t pol = l2_policy_evict_last();  // a prompt's tiles re-read the same pages
+    for (;;) {
+        if (lane == 0) *c.sUnit = atomicAdd(p.sched, 1);
+        __syncthreads();  // (1)
+        const int u = *c.sUnit;
+        if (u >= c.nunits || *c.abort_flag) break;
+        const int g = u % p.kv_heads;
+        __syncthreads();  // (2)
+        {  // runs: one per table row among the valid tokens, in order of first token;
+           // lane l holds tokens l and l + 32
+            const int pa = c.sPos[lane], pb = c.sPos[lane + 32];
+            const int ra = c.sRow[lane], rb = c.sRow[lane + 32];
+            bool ua = pa >= 0, ub = pb >= 0;  // valid tokens not yet in a run
+            int nr = 0;
+            for (;;) {
+                const uint32_t ma = __ballot_sync(kAll, ua), mb = __ballot_sync(kAll, ub);
+                if (!ma && !mb) break;
+                const int r = ma ? __shfl_sync(kAll, ra, __ffs(ma) - 1) : __shfl_sync(kAll, rb, __ffs(mb) - 1);
+                const bool ia = ua && ra == r, ib = ub && rb == r;
+                const int n = (int)__reduce_max_sync(
+                    kAll, (uint32_t)max(ia ? pa / kPageSize + 1 : 0, ib ? pb / kPageSize + 1 : 0));
+                if (lane == 0) {
+                    c.sRunRow[nr] = r;
+                    c.sRunPages[nr] = n;
+                }
+                ua = ua && !ia;
+                ub = ub && !ib;
                 ++nr;
             }
-            sRunPages[r] = max(sRunPages[r], sPos[i] / kPageSize + 1);
+            if (lane == 0) *c.sNumRuns = nr;
         }
-        *sNumRuns = nr;
-    }
-
-    // ---- Q: QK-norm + RoPE of (head 4g + warp, token lane), scaled by log2(e)/sqrt(128), bf16
-    if (warp < kSoftmaxWarps) {
-        const int m = tid;  // tile row
-        const int pos = sPos[lane];
-        uint8_t* q0 = sbase + L::kQ;
-        if (pos >= 0) {
-            // two passes over the row (the second from L1): sum of squares, then norm + rotate
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.q + ((int64_t)(p0 + lane) * p.heads + g * kGroup + warp) * kHeadDim);
-            const uint4* wsm = reinterpret_cast<const uint4*>(sbase + L::kW);
-            const float2* rp = p.rope_hi + (int64_t)pos * kRopeHalf;
-            float ss = 0.f;
-#pragma unroll
-            for (int c = 0; c < kHeadDim / 8; ++c) {
-                const uint4 r = src[c];
-                const uint32_t rv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = __uint_as_float(rv[e] << 16), b = __uint_as_float(rv[e] & 0xffff0000u);
-                    ss += a * a + b * b;
-                }
-            }
-            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * (1.4426950408889634f * 0.088388347648318440f);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {  // dims 8c..8c+7 of the first half and their partners 64 apart
-                const uint4 rl = src[c], rh = src[c + 8], wl = wsm[c], wh = wsm[c + 8];
-                const uint32_t xl[4] = {rl.x, rl.y, rl.z, rl.w}, xh[4] = {rh.x, rh.y, rh.z, rh.w};
-                const uint32_t vl[4] = {wl.x, wl.y, wl.z, wl.w}, vh[4] = {wh.x, wh.y, wh.z, wh.w};
-                uint32_t lo[4], hi[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float y[2], z[2];
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int d = 8 * c + 2 * e + b;
-                        const float ul = __uint_as_float(b ? (xl[e] & 0xffff0000u) : (xl[e] << 16)) *
-                                         __uint_as_float(b ? (vl[e] & 0xffff0000u) : (vl[e] << 16));
-                        const float uh = __uint_as_float(b ? (xh[e] & 0xffff0000u) : (xh[e] << 16)) *
-                                         __uint_as_float(b ? (vh[e] & 0xffff0000u) : (vh[e] << 16));
-                        const float2 cs = rp[d];
-                        y[b] = inv * (ul * cs.x - uh * cs.y);  // y[d]      = u[d] cos - u[d+64] sin
-                        z[b] = inv * (uh * cs.x + ul * cs.y);  // y[d + 64] = u[d+64] cos + u[d] sin
-                    }
-                    lo[e] = pack_bf16(__float2bfloat16_rn(y[0]), __float2bfloat16_rn(y[1]));
-                    hi[e] = pack_bf16(__float2bfloat16_rn(z[0]), __float2bfloat16_rn(z[1]));
-                }
-                *reinterpret_cast<uint4*>(q0 + sw128(m, 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                *reinterpret_cast<uint4*>(q0 + kTileRows * 128 + sw128(m, 8 * c)) =
-                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                *reinterpret_cast<uint4*>(q0 + sw128(m, 8 * c)) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(q0 + kTileRows * 128 + sw128(m, 8 * c)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q is read by the tensor cores
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
-    const int nruns = *sNumRuns;
-
-    if (warp == kProducer) {
-        // ================================================================ producer
-        const uint64_t pol = l2_policy_evict_last();  // a prompt's tiles re-read the same pages
-        int i = 0;
+        __syncthreads();  // (3)
+        const int nruns = *c.sNumRuns;
         bool ok = true;
         for (int r = 0; r < nruns && ok; ++r) {
-            const int row = sRunRow[r];
-            const int n = sRunPages[r];
+            const int row = c.sRunRow[r];
+            const int n = c.sRunPages[r];
             for (int b0 = 0; b0 < n && ok; b0 += 32) {
                 const int mine = (b0 + lane < n) ? page_of(p.table, p.pages, row, b0 + lane) : 0;
-                for (int jj = 0; jj < min(32, n - b0); ++jj, ++i) {
-                    const int page = __shfl_sync(kAll, mine, jj);
-                    const int st = i % kPfStages;
-                    if (i >= kPfStages && (!mbar_wait(bar_empty + 8 * st, ((i / kPfStages) - 1) & 1) || *abort_flag)) {
-                        ok = false;
-                        break;
+                for (int jj = 0; jj < min(32, n - b0) && ok; jj += 2) {
+                    const int npg = min(2, n - b0 - jj);
+                    const int pg0 = __shfl_sync(kAll, mine, jj);
+                    const int pg1 = __shfl_sync(kAll, mine, jj + 1);
+                    for (int kind = 0; kind < 2 && ok; ++kind) {  // the block's K, then its V
+                        const int st = q_load % kPfStages;
+                        if (q_load >= kPfStages)
+                            ok = __all_sync(kAll, mbar_wait(c.bar_empty + 8 * st, ((q_load / kPfStages) - 1) & 1) &&
+                                                      !*c.abort_flag);
+                        if (!ok) break;
+                        if (lane == 0) {
+                            const CUtensorMap* tm = kind ? tmV : tmK;
+                            const uint32_t fb = c.bar_full + 8 * st;
+                            const uint32_t dst = c.base + PfSmem::kRing + st * kPfStageBytes;
+                            mbar_arrive_expect_tx(fb, npg * 2 * kPageSize * 128);
+                            for (int i = 0; i < npg; ++i) {
+                                const int y = (i ? pg1 : pg0) * kPageSize;
+                                tma_load_3d(dst + i * (kPageSize * 128), tm, 0, y, g, fb, pol);
+                                tma_load_3d(dst + kHalfBytes + i * (kPageSize * 128), tm, 64, y, g, fb, pol);
+                            }
+                        }
+                        ++q_load;
+                        __syncwarp();
                     }
-                    if (lane == 0) {
-                        const uint32_t fb = bar_full + 8 * st, dst = base + L::kRing + st * kPfStageBytes;
-                        mbar_arrive_expect_tx(fb, kPfStageBytes);
-                        const int y = page * kPageSize;
-                        tma_load_3d(dst, &tmK, 0, y, g, fb, pol);
-                        tma_load_3d(dst + 8192, &tmK, 64, y, g, fb, pol);
-                        tma_load_3d(dst + 16384, &tmV, 0, y, g, fb, pol);
-                        tma_load_3d(dst + 24576, &tmV, 64, y, g, fb, pol);
-                    }
-                    __syncwarp();
                 }
             }
         }
         if (!ok && lane == 0) {
             atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            for (int k = max(0, i - kPfStages); k < i; ++k)
-                mbar_wait(bar_full + 8 * (k % kPfStages), (k / kPfStages) & 1);
+            *c.abort_flag = 1;
+            // let the copies in flight land before the CTA ends
+            for (int k = max(0, q_load - kPfStages); k < q_load; ++k)
+                mbar_wait(c.bar_full + 8 * (k % kPfStages), (k / kPfStages) & 1);
         }
-    } else if (warp == kIssuer) {
-        // ================================================================ MMA issuer
+        __syncthreads();  // (4)
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer (warp 9, one thread)
+__device__ __forceinline__ void issuer_role(const PfCtx& c, const PfParams& p, int lane)
+{
+    const uint32_t qb = c.base + PfSmem::kQ, ring = c.base + PfSmem::kRing;
+    const uint32_t tmem = c.tmem;
+    int q_use = 0, it = 0, rc = 0;  // ring loads, blocks and runs so far, across units
+    for (;;) {
+        __syncthreads();  // (1)
+        if (*c.sUnit >= c.nunits || *c.abort_flag) break;
+        __syncthreads();  // (2)
+        tc_fence_before();
+        __syncthreads();  // (3)
+        tc_fence_after();
+        const int nruns = *c.sNumRuns;
         if (lane == 0) {
-            constexpr uint32_t id_qk = umma_idesc_bf16(kTileRows, kPageSize, 0, 0);
-            constexpr uint32_t id_pv = umma_idesc_bf16(kTileRows, kHeadDim, 0, 1);
-            const uint32_t qb = base + L::kQ, pb = base + L::kP;
             bool ok = true;
-            int jg = 0;
             for (int r = 0; r < nruns && ok; ++r) {
-                const int n = sRunPages[r];
-                for (int jj = 0; jj <= n && ok; ++jj) {
-                    if (jj < n) {  // S_j = Q K_j^T
-                        const int j = jg + jj, st = j % kPfStages, sb = j & 1;
-                        if (!mbar_wait(bar_full + 8 * st, (j / kPfStages) & 1) || *abort_flag) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t kst = base + L::kRing + st * kPfStageBytes;
-#pragma unroll
-                        for (int k = 0; k < kHeadDim / 16; ++k) {
-                            const uint64_t a = umma_desc_sw128(qb + (k >> 2) * (kTileRows * 128) + (k & 3) * 32, 16, 1024);
-                            const uint64_t b = umma_desc_sw128(kst + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-                            umma_bf16(tmem + sb * kPageSize, a, b, id_qk, k > 0);
-                        }
-                        umma_commit(bar_s + 8 * sb);
+                const int n = c.sRunPages[r];
+                const int nb = (n + 1) / 2;
+                {  // S_0(0), S_1(0)
+                    const int st = q_use % kPfStages;
+                    if (!mbar_wait_spin(c.bar_full + 8 * st, (q_use / kPfStages) & 1) || *c.abort_flag) {
+                        ok = false;
+                        break;
                     }
-                    if (jj >= 1) {  // O += P_{j-1} V_{j-1}
-                        const int j = jg + jj - 1, st = j % kPfStages, sb = j & 1;
-                        if (!mbar_wait(bar_p + 8 * sb, (j >> 1) & 1) ||
-                            (jj == 1 && r > 0 && !mbar_wait(bar_epi, (r - 1) & 1)) || *abort_flag) {
+                    tc_fence_after();
+                    const uint32_t kst = ring + st * kPfStageBytes;
+                    issue_s(tmem, qb, kst, c.bar_s, 0, min(2, n));
+                    issue_s(tmem, qb, kst, c.bar_s, 1, min(2, n));
+                    umma_commit(c.bar_empty + 8 * st);
+                }
+                for (int b = 0; b < nb && ok; ++b) {
+                    const int j = it + b;
+                    const int vq = q_use + 2 * b + 1, vst = vq % kPfStages;
+                    const int kq = vq + 1, kst = kq % kPfStages;
+                    const int npg = min(2, n - 2 * b);
+                    const bool more = b + 1 < nb;
+                    if (!mbar_wait_spin(c.bar_full + 8 * vst, (vq / kPfStages) & 1) || *c.abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vs = ring + vst * kPfStageBytes;
+                    for (int h = 0; h < kGroups; ++h) {
+                        // O_h += P_h V_b once the softmax has written P_h (and, at a run's
+                        // first block, the previous run's epilogue has read O_h)
+                        if (!mbar_wait_spin(c.bar_p + 8 * h, j & 1) ||
+                            (b == 0 && r > 0 && !mbar_wait_spin(c.bar_epi + 8 * h, (rc + r - 1) & 1)) ||
+                            *c.abort_flag) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t vst = base + L::kRing + st * kPfStageBytes + 16384;
-#pragma unroll
-                        for (int k = 0; k < kPageSize / 16; ++k) {
-                            const uint64_t a = umma_desc_sw128(pb + sb * (kTileRows * 128) + k * 32, 16, 1024);
-                            const uint64_t b = umma_desc_sw128(vst + k * 2048, 8192, 1024);
-                            umma_bf16(tmem + 2 * kPageSize, a, b, id_pv, jj > 1 || k > 0);
+                        issue_pv(tmem, vs, h, npg, b > 0);
+                        umma_commit(c.bar_o + 8 * h);
+                        if (h == kGroups - 1) umma_commit(c.bar_empty + 8 * vst);
+                        if (more) {  // S_h(b+1) over P_h(b), after the product that reads it
+                            if (h == 0) {
+                                if (!mbar_wait_spin(c.bar_full + 8 * kst, (kq / kPfStages) & 1) || *c.abort_flag) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            issue_s(tmem, qb, ring + kst * kPfStageBytes, c.bar_s, h, min(2, n - 2 * b - 2));
+                            if (h == kGroups - 1) umma_commit(c.bar_empty + 8 * kst);
                         }
-                        umma_commit(bar_o + 8 * sb);
-                        umma_commit(bar_empty + 8 * st);
                     }
                 }
-                jg += n;
+                it += nb;
+                q_use += 2 * nb;
             }
             if (!ok) {
                 atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-                *abort_flag = 1;
+                *c.abort_flag = 1;
             }
         }
-        __syncwarp();
-    } else {
-        // ================================================================ softmax warps
-        const int m = tid;                 // tile row: head `warp` of the group, token `lane`
-        const int pos = sPos[lane];
-        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-        uint8_t* pbuf = sbase + L::kP;
+        q_use = __shfl_sync(kAll, q_use, 0);
+        it = __shfl_sync(kAll, it, 0);
+        rc += nruns;
+        tc_fence_before();
+        __syncthreads();  // (4)
+        tc_fence_after();
+    }
+    if (lane == 0) {  // every product this thread issued has completed before the columns are freed
+        umma_commit(c.bar_drain);
+        mbar_wait_spin(c.bar_drain, 0);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- softmax group h (warps 4h..4h+3)
+// Thread (warp w, lane) owns row 32 (w % 4) + lane of its group: query head
+// 4g + w % 4 of token 32h + lane of the tile.
+__device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, int tid, int lane, int warp)
+{
+    const int h = warp >> 2, wq = warp & 3;
+    const int tok = kHalfTok * h + lane;
+    const uint32_t tl = c.tmem + ((uint32_t)(wq * 32) << 16) + 256 * h;  // S/P; O at +128
+    int it = 0;  // blocks so far, across units
+    for (;;) {
+        __syncthreads();  // (1)
+        const int u = *c.sUnit;
+        if (u >= c.nunits || *c.abort_flag) break;
+        const int g = u % p.kv_heads;
+        const int p0 = tile_of(c, p, u) * kTileTok;
+        if (tid < kTileTok) {  // the tile's tokens
+            const int t = p0 + tid;
+            const int len = t < p.P ? p.tok_len[t] : 0;
+            c.sPos[tid] = len - 1;  // -1: not a token, or skipped
+            c.sRow[tid] = len > 0 ? p.tok_row[t] : -1;
+        }
+        __syncthreads();  // (2)
+        const int pos = c.sPos[tok];
+        {  // stage the valid tokens' q rows (the 4 heads of g) and RoPE rows in the idle
+           // ring, coalesced: flat 16-byte chunk f of token f / 96 (64 chunks of q, 32 of
+           // RoPE).  Chunk w of token t sits at position w ^ (t % 8) of the token's row, so
+           // that both these writes and the per-row reads below are free of bank conflicts.
+            constexpr int kChunks = kTileTok * 96, kPer = kChunks / (32 * 4 * kGroups);
+            uint4 r[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int f = tid + (32 * 4 * kGroups) * i, t = f / 96, w = f % 96;
+                const int tp = c.sPos[t];
+                r[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (tp >= 0)
+                    r[i] = w < 64 ? reinterpret_cast<const uint4*>(
+                                        p.q + ((int64_t)(p0 + t) * p.heads + g * kGroup) * kHeadDim)[w]
+                                  : reinterpret_cast<const uint4*>(p.rope_hi + (int64_t)tp * kRopeHalf)[w - 64];
+            }
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int f = tid + (32 * 4 * kGroups) * i, t = f / 96, w = f % 96;
+                const int off = w < 64 ? PfSmem::kStageQ + t * 1024 + 16 * (w ^ (t & 7))
+                                       : PfSmem::kStageRope + t * 512 + 16 * ((w - 64) ^ (t & 7));
+                *reinterpret_cast<uint4*>(c.sbase + off) = r[i];
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * 4 * kGroups) : "memory");  // the softmax warps only
+        }
+        const int64_t qrow = ((int64_t)(p0 + tok) * p.heads + g * kGroup + wq) * kHeadDim;
+
+        // ---- Q: QK-norm + RoPE of this row, scaled by log2(e)/sqrt(128), bf16, swizzled
+        {
+            const int m = tid & (kRowsM - 1);
+            uint8_t* q0 = c.sbase + PfSmem::kQ + h * (2 * kRowsM * 128);
+            if (pos >= 0) {
+                // from the staged rows (chunk j of this row at position j ^ (tok % 8))
+                const uint8_t* qs = c.sbase + PfSmem::kStageQ + tok * (kGroup * kHeadDim * 2);
+                const uint8_t* rs = c.sbase + PfSmem::kStageRope + tok * (kRopeHalf * 8);
+                const int sw = tok & 7;
+                auto qchunk = [&](int k) {
+                    return *reinterpret_cast<const uint4*>(qs + 16 * ((wq * 16 + k) ^ sw));
+                };
+                const uint4* wsm = reinterpret_cast<const uint4*>(c.sbase + PfSmem::kW);
+                float ss = 0.f;
+#pragma unroll
+                for (int k = 0; k < kHeadDim / 8; ++k) {
+                    const uint4 r = qchunk(k);
+                    const uint32_t rv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = __uint_as_float(rv[e] << 16), b = __uint_as_float(rv[e] & 0xffff0000u);
+                        ss += a * a + b * b;
+                    }
+                }
+                const float inv =
+                    rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * (1.4426950408889634f * 0.088388347648318440f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // dims 8k..8k+7 of the first half and their partners 64 apart
+                    const uint4 rl = qchunk(k), rh = qchunk(k + 8);
+                    const uint4 wl = wsm[k], wh = wsm[k + 8];
+                    const uint32_t xl[4] = {rl.x, rl.y, rl.z, rl.w}, xh[4] = {rh.x, rh.y, rh.z, rh.w};
+                    const uint32_t vl[4] = {wl.x, wl.y, wl.z, wl.w}, vh[4] = {wh.x, wh.y, wh.z, wh.w};
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float y[2], z[2];
+                        const float4 cc =  // (cos, sin) of dims 8k + 2e and 8k + 2e + 1
+                            *reinterpret_cast<const float4*>(rs + 16 * ((4 * k + e) ^ sw));
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const float ul = __uint_as_float(b ? (xl[e] & 0xffff0000u) : (xl[e] << 16)) *
+                                             __uint_as_float(b ? (vl[e] & 0xffff0000u) : (vl[e] << 16));
+                            const float uh = __uint_as_float(b ? (xh[e] & 0xffff0000u) : (xh[e] << 16)) *
+                                             __uint_as_float(b ? (vh[e] & 0xffff0000u) : (vh[e] << 16));
+                            const float co = b ? cc.z : cc.x, si = b ? cc.w : cc.y;
+                            y[b] = inv * (ul * co - uh * si);  // y[d]      = u[d] cos - u[d+64] sin
+                            z[b] = inv * (uh * co + ul * si);  // y[d + 64] = u[d+64] cos + u[d] sin
+                        }
+                        const __nv_bfloat162 yl = __floats2bfloat162_rn(y[0], y[1]);
+                        const __nv_bfloat162 zh = __floats2bfloat162_rn(z[0], z[1]);
+                        lo[e] = *reinterpret_cast<const uint32_t*>(&yl);
+                        hi[e] = *reinterpret_cast<const uint32_t*>(&zh);
+                    }
+                    *reinterpret_cast<uint4*>(q0 + sw128(m, 8 * k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(q0 + kRowsM * 128 + sw128(m, 8 * k)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    *reinterpret_cast<uint4*>(q0 + sw128(m, 8 * k)) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(q0 + kRowsM * 128 + sw128(m, 8 * k)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q is read by the tensor cores
+        }
+        tc_fence_before();
+        __syncthreads();  // (3)
+        tc_fence_after();
+        const int nruns = *c.sNumRuns;
+
+        __nv_bfloat16* dst_row = p.out + qrow;
         bool ok = true;
-        int jg = 0;
         for (int r = 0; r < nruns && ok; ++r) {
-            const int n = sRunPages[r];
-            const bool active = pos >= 0 && sRow[lane] == sRunRow[r];
+            const int n = c.sRunPages[r];
+            const int nb = (n + 1) / 2;
+            const bool active = pos >= 0 && c.sRow[tok] == c.sRunRow[r];
             float m_used = -CUDART_INF_F, l = 0.f;
-            for (int jj = 0; jj < n; ++jj) {
-                const int j = jg + jj, sb = j & 1;
-                if (!mbar_wait(bar_s + 8 * sb, (j >> 1) & 1) || *abort_flag) {
+            for (int b = 0; b < nb; ++b) {
+                const int j = it + b;
+                if (!mbar_wait_spin(c.bar_s + 8 * h, j & 1) || *c.abort_flag) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                float s[kPageSize];
-                {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tl + sb * kPageSize, v0);
-                    tmem_ld32(tl + sb * kPageSize + 32, v1);
-                    tmem_wait_ld();
+                // S of the block (a one-page block leaves columns 64..127 stale: the causal
+                // mask removes them, every position of the run lies below its last page)
+                const int lim = active ? pos - b * kBlockKeys : -1;  // keys c <= lim are visible
+                const bool full = __all_sync(kAll, lim >= kBlockKeys - 1);
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(tl, v0);
+                tmem_ld32(tl + 32, v1);
+                tmem_ld32(tl + 64, v2);
+                tmem_ld32(tl + 96, v3);
+                tmem_wait_ld_regs(v0);
+                tmem_wait_ld_regs(v1);
+                tmem_wait_ld_regs(v2);
+                tmem_wait_ld_regs(v3);
+                if (!full) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        s[c] = __uint_as_float(v0[c]);
-                        s[c + 32] = __uint_as_float(v1[c]);
+                    for (int k = 0; k < 32; ++k) {
+                        if (k > lim) v0[k] = __float_as_uint(-CUDART_INF_F);
+                        if (32 + k > lim) v1[k] = __float_as_uint(-CUDART_INF_F);
+                        if (64 + k > lim) v2[k] = __float_as_uint(-CUDART_INF_F);
+                        if (96 + k > lim) v3[k] = __float_as_uint(-CUDART_INF_F);
                     }
                 }
-                // causal mask: keys up to pos; only a page that reaches past pos needs it
-                const int first = jj * kPageSize;
-                if (!active || first > pos) {
+                float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-                    for (int c = 0; c < kPageSize; ++c) s[c] = -CUDART_INF_F;
-                } else if (first + kPageSize - 1 > pos) {
-#pragma unroll
-                    for (int c = 0; c < kPageSize; ++c)
-                        if (first + c > pos) s[c] = -CUDART_INF_F;
-                }
-                float mx4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-                for (int c = 4; c < kPageSize; c += 4) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], s[c + e]);
-                }
+                for (int k = 0; k < 32; ++k)
+                    mx4[k & 3] = fmaxf(mx4[k & 3], fmaxf(fmaxf(__uint_as_float(v0[k]), __uint_as_float(v1[k])),
+                                                         fmaxf(__uint_as_float(v2[k]), __uint_as_float(v3[k]))));
                 const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                // move the running max (rescaling O and l) only when this page raises it by > 8
+                // move the running max (rescaling O and l) only when this block raises it by > 8
                 bool need = false;
                 float alpha = 1.f;
-                if (jj == 0) {
+                if (b == 0) {
                     m_used = mx;
                 } else if (mx > m_used + kRescale) {
                     need = true;
                     alpha = exp2f(m_used - mx);
                 }
                 if (__any_sync(kAll, need)) {
-                    const int jp = j - 1;  // O must hold the previous page's product first
-                    if (!mbar_wait(bar_o + 8 * (jp & 1), (jp >> 1) & 1)) {
+                    // O must hold the previous block's product first
+                    if (!mbar_wait_spin(c.bar_o + 8 * h, (j - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < kHeadDim; c += 16) {
+                    for (int k = 0; k < kHeadDim; k += 16) {
                         uint32_t v[16];
-                        tmem_ld16(tl + 2 * kPageSize + c, v);
+                        tmem_ld16(tl + 128 + k, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st16(tl + 2 * kPageSize + c, v);
+                        tmem_st16(tl + 128 + k, v);
                     }
                     tmem_wait_st();
                     if (need) {
@@ -379,80 +541,193 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         m_used = mx;
                     }
                 }
-                // P_j = 2^(S_j - m): into P buffer sb once the product two pages back has read it
-                // (a row with no key yet has m = -inf: its p are all 0)
+                // P = 2^(S - m) as bf16 pairs over the first half of S (a row with no key
+                // yet has m = -inf: its p are all 0)
                 const float msub = m_used == -CUDART_INF_F ? 0.f : m_used;
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[kPageSize / 2];
+                auto p_chunk = [&](const uint32_t (&v)[32], int cc) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < kPageSize; c += 2) {
-                    const float a = ex2_approx(s[c] - msub);
-                    const float b = ex2_approx(s[c + 1] - msub);
-                    ps4[(c >> 1) & 3] += a + b;
-                    __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
-                    pk[c / 2] = *reinterpret_cast<uint32_t*>(&ab);
-                }
+                    for (int e = 0; e < 32; e += 2) {
+                        const float a = ex2_approx(__uint_as_float(v[e]) - msub);
+                        const float bb = ex2_approx(__uint_as_float(v[e + 1]) - msub);
+                        ps4[(e >> 1) & 3] += a + bb;
+                        const __nv_bfloat162 ab = __floats2bfloat162_rn(a, bb);  // one paired conversion
+                        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&ab);
+                    }
+                    tmem_st16(tl + 16 * cc, pk);
+                };
+                p_chunk(v0, 0);
+                p_chunk(v1, 1);
+                p_chunk(v2, 2);
+                p_chunk(v3, 3);
                 l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-                if (j >= 2 && !mbar_wait(bar_o + 8 * sb, ((j - 2) >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* prow = pbuf + sb * (kTileRows * 128);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(prow + sw128(m, 8 * c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P is read by the tensor cores
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_p + 8 * sb);
+                if (lane == 0) mbar_arrive(c.bar_p + 8 * h);
             }
             if (!ok) break;
             // ---- epilogue of this row's pass: O / l for the active rows
-            const int jl = jg + n - 1;
-            if (!mbar_wait(bar_o + 8 * (jl & 1), (jl >> 1) & 1)) {
+            if (!mbar_wait_spin(c.bar_o + 8 * h, (it + nb - 1) & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            __nv_bfloat16* dst = p.out + ((int64_t)(p0 + lane) * p.heads + g * kGroup + warp) * kHeadDim;
             const float inv = active ? 1.f / l : 0.f;
 #pragma unroll
-            for (int c = 0; c < kHeadDim; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tl + 2 * kPageSize + c, v);
-                tmem_wait_ld();
+            for (int k0 = 0; k0 < kHeadDim; k0 += 64) {
+                uint32_t va[32], vb[32];
+                tmem_ld32(tl + 128 + k0, va);
+                tmem_ld32(tl + 128 + k0 + 32, vb);
+                tmem_wait_ld_regs(va);
+                tmem_wait_ld_regs(vb);
                 if (active) {
-                    uint32_t o8[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        o8[e] = pack_bf16(__float2bfloat16_rn(__uint_as_float(v[2 * e]) * inv),
-                                          __float2bfloat16_rn(__uint_as_float(v[2 * e + 1]) * inv));
-                    *reinterpret_cast<uint4*>(dst + c) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-                    *reinterpret_cast<uint4*>(dst + c + 8) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+                    for (int k = 0; k < 64; k += 8) {
+                        const uint32_t* v = k < 32 ? va + k : vb + (k - 32);
+                        uint32_t o4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 o2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]) * inv,
+                                                                            __uint_as_float(v[2 * e + 1]) * inv);
+                            o4[e] = *reinterpret_cast<const uint32_t*>(&o2);
+                        }
+                        *reinterpret_cast<uint4*>(dst_row + k0 + k) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_epi);
-            jg += n;
+            if (lane == 0) mbar_arrive(c.bar_epi + 8 * h);
+            it += nb;
         }
         // skipped tokens of the tile: zero output
-        if (pos < 0 && p0 + lane < p.P) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(p0 + lane) * p.heads + g * kGroup + warp) * kHeadDim);
+        if (ok && pos < 0 && p0 + tok < p.P) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row);
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            for (int k = 0; k < kHeadDim / 8; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
         }
         if (!ok && lane == 0) {
             atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-            *abort_flag = 1;
+            *c.abort_flag = 1;
+        }
+        tc_fence_before();
+        __syncthreads();  // (4)
+        tc_fence_after();
+    }
+}
+
+// ---------------------------------------------------------------- warps 10 and 11
+__device__ __forceinline__ void idle_role(const PfCtx& c)
+{
+    for (;;) {
+        __syncthreads();  // (1)
+        if (*c.sUnit >= c.nunits || *c.abort_flag) break;
+        __syncthreads();  // (2)
+        __syncthreads();  // (3)
+        __syncthreads();  // (4)
+    }
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, PfParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    PfCtx c;
+    c.base = (raw_base + 1023u) & ~1023u;
+    c.sbase = smem_raw + (c.base - raw_base);
+    const uint32_t bar0 = c.base + PfSmem::kBars;
+    c.bar_full = bar0;
+    c.bar_empty = bar0 + 8 * kPfStages;
+    c.bar_s = bar0 + 16 * kPfStages;
+    c.bar_p = c.bar_s + 8 * kGroups;
+    c.bar_o = c.bar_p + 8 * kGroups;
+    c.bar_epi = c.bar_o + 8 * kGroups;
+    c.bar_drain = c.bar_epi + 8 * kGroups;
+    uint32_t* sKey = reinterpret_cast<uint32_t*>(c.sbase + PfSmem::kSort);
+    c.sKey = sKey;
+    c.sPos = reinterpret_cast<int*>(c.sbase + PfSmem::kTok);
+    c.sRow = c.sPos + kTileTok;
+    c.sRunRow = reinterpret_cast<int*>(c.sbase + PfSmem::kRuns);
+    c.sRunPages = c.sRunRow + kTileTok;
+    c.sNumRuns = c.sRunPages + kTileTok;
+    c.sUnit = c.sNumRuns + 1;
+    c.abort_flag = reinterpret_cast<volatile int*>(c.sbase + PfSmem::kFlag);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2 * kPfStages; ++i) mbar_init(bar0 + 8 * i, 1);  // full (producer), empty (commit)
+        for (int h = 0; h < kGroups; ++h) {
+            mbar_init(c.bar_s + 8 * h, 1);
+            mbar_init(c.bar_p + 8 * h, 4);
+            mbar_init(c.bar_o + 8 * h, 1);
+            mbar_init(c.bar_epi + 8 * h, 4);
+        }
+        mbar_init(c.bar_drain, 1);
+        *c.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kIssuer) tmem_alloc(c.base + PfSmem::kTmemSlot, kTmemCols);
+    if (warp == kProducer && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    pdl_wait();  // prep_kernel's appends, token table and zeroed unit counter
+
+    // ---- unit order: tiles by decreasing page count, ties in token order
+    const int ntiles = p.ntiles;
+    c.sorted = ntiles <= kMaxSortTiles;
+    c.nunits = ntiles * p.kv_heads;
+    if (tid < kHeadDim / 4)
+        reinterpret_cast<uint2*>(c.sbase + PfSmem::kW)[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
+    if (c.sorted) {
+        int n2 = 1;
+        while (n2 < ntiles) n2 <<= 1;
+        for (int i = tid; i < n2; i += kPfThreads) sKey[i] = 0;
+        __syncthreads();
+        for (int t = tid; t < p.P; t += kPfThreads) {
+            const int len = p.tok_len[t];
+            if (len > 0) atomicMax(&sKey[t / kTileTok], (uint32_t)((len - 1) / kPageSize + 1));
+        }
+        __syncthreads();
+        for (int i = tid; i < ntiles; i += kPfThreads)
+            sKey[i] = (sKey[i] << kSortIdxBits) | (uint32_t)((kMaxSortTiles - 1) - i);
+        __syncthreads();
+        for (int k = 2; k <= n2; k <<= 1) {  // bitonic sort, descending
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < n2; i += kPfThreads) {
+                    const int ixj = i ^ j;
+                    if (ixj > i) {
+                        const uint32_t a = sKey[i], b = sKey[ixj];
+                        if (((i & k) == 0) ? (a < b) : (a > b)) {
+                            sKey[i] = b;
+                            sKey[ixj] = a;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kIssuer) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+    tc_fence_after();
+    c.tmem = *reinterpret_cast<volatile uint32_t*>(c.sbase + PfSmem::kTmemSlot);
+
+    if (warp >= kProducer) {
+        regs_dec<kRegsOther>();
+        if (warp == kProducer)
+            producer_role(c, p, &tmK, &tmV, lane);
+        else if (warp == kIssuer)
+            issuer_role(c, p, lane);
+        else
+            idle_role(c);
+    } else {
+        regs_inc<kRegsSoftmax>();
+        softmax_role(c, p, tid, lane, warp);
     }
 }
 
@@ -460,6 +735,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 cudaError_t configure_prefill()
 {
+    // The kernel moves registers between its warpgroups assuming it is launched
+    // with exactly kRegsLaunch per thread; refuse to run it with any other count.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != (int)kRegsLaunch) return cudaErrorInvalidConfiguration;
     return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem::kAlloc);
 }
 
@@ -473,6 +754,7 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.table = a.table;
     p.rope_hi = pool->rope_hi;
     p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.sched = reinterpret_cast<int32_t*>(a.ws + plan.off_sched);
     p.err = pool->err;
     p.P = a.P;
     p.pages = a.pages;
@@ -480,8 +762,9 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.kv_heads = pool->cfg.kv_heads;
     p.ntiles = (a.P + kTileTok - 1) / kTileTok;
     p.eps = static_cast<float>(pool->cfg.eps);
+    const int units = p.ntiles * p.kv_heads;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.ntiles * p.kv_heads));
+    cfg.gridDim = dim3((unsigned)(units < pool->num_sms ? units : pool->num_sms));
     cfg.blockDim = dim3(kPfThreads);
     cfg.dynamicSmemBytes = PfSmem::kAlloc;
     cfg.stream = s;

@@ -48,25 +48,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Gives up
-// after roughly a second of polling and returns false.
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // every wait gives up after one second
+
+// Bounded wait for the phase with the given parity to complete, sleeping
+// between polls (for waits on copies from memory).  Gives up after a second
+// and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    for (uint32_t it = 0; it < (1u << 22); ++it) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
         __nanosleep(128);
         if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     }
-    return false;
 }
 
 // Bounded wait without sleeping, for short waits among the warps of one CTA
 // (try_wait itself suspends the thread for a while when the phase is open).
+// Gives up after a second and returns false.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
 {
-    for (uint32_t it = 0; it < (1u << 26); ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
+        if ((it & 1023u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // ---- TMA ----------------------------------------------------------------------
@@ -158,6 +173,35 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t 
         "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
 }
 
+// D(tmem) (+)= A(tmem) * B(smem): A is M rows (one per lane) x K bf16, two
+// elements to a 32-bit column, starting at column address `tmem_a`.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                             bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+// The same two products with the accumulate flag given as a predicate the
+// caller computes once, for issue loops where every cycle of the issuing
+// thread counts.
+__device__ __forceinline__ void umma_bf16_acc(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc));
+}
+__device__ __forceinline__ void umma_bf16_ts_acc(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc));
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
@@ -217,6 +261,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// tcgen05.wait::ld that also ties the 32 destination registers of an earlier
+// load, so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
 // 2^x on the special-function unit (approximate, flushes denormals; 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x)
 {
@@ -232,6 +290,20 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+// ---- per-warpgroup register budget -----------------------------------------------------
+// Executed by all four warps of a warpgroup; the sums over warpgroups must stay
+// within the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---- programmatic dependent launch -----------------------------------------------------
