@@ -66,7 +66,8 @@ static_assert(kRegsLaunch * kPfThreads <= 65536, "register file");
 constexpr uint32_t kTmemCols = 512;            // group h: S/P at 256h, O at 256h + 128
 constexpr float kRescale = 8.f;                // log2 headroom before the running max moves
 constexpr int kMaxSortTiles = 2048;            // larger calls take tiles in token order
-constexpr int kSortIdxBits = 11;
+// sort key of a work item (tile, run): pages << 17 | (2047 - tile) << 6 | (63 - run)
+constexpr int kKeyTileShift = 6, kKeyPagesShift = 17;
 
 struct PfSmem {
     static constexpr int kQ = 0;                                    // 2 groups x [2 halves][128 rows][128 B]
@@ -126,10 +127,42 @@ struct PfCtx {
     bool sorted;
 };
 
-__device__ __forceinline__ int tile_of(const PfCtx& c, const PfParams& p, int u)
+// Work unit u: kv head u % G of item u / G; an item is one run (table row) of
+// a tile when the items are sorted, else a whole tile (every run, run = -1).
+__device__ __forceinline__ void item_of(const PfCtx& c, const PfParams& p, int u, int& tile, int& run)
 {
-    return c.sorted ? (kMaxSortTiles - 1) - (int)(c.sKey[u / p.kv_heads] & ((1u << kSortIdxBits) - 1))
-                    : u / p.kv_heads;
+    if (c.sorted) {
+        const uint32_t key = c.sKey[u / p.kv_heads];
+        tile = (kMaxSortTiles - 1) - (int)((key >> kKeyTileShift) & (kMaxSortTiles - 1));
+        run = 63 - (int)(key & 63);
+    } else {
+        tile = u / p.kv_heads;
+        run = -1;
+    }
+}
+
+// The runs of a tile (one per table row among its valid tokens, in order of
+// first token) computed by one warp; lane l holds tokens l and l + 32 with
+// positions pa, pb and rows ra, rb (position < 0: not a token).  For each run
+// calls emit(index, row, pages) on every lane; returns the number of runs.
+template <typename Emit>
+__device__ __forceinline__ int tile_runs(int pa, int pb, int ra, int rb, Emit emit)
+{
+    bool ua = pa >= 0, ub = pb >= 0;  // valid tokens not yet in a run
+    int nr = 0;
+    for (;;) {
+        const uint32_t ma = __ballot_sync(kAll, ua), mb = __ballot_sync(kAll, ub);
+        if (!ma && !mb) break;
+        const int r = ma ? __shfl_sync(kAll, ra, __ffs(ma) - 1) : __shfl_sync(kAll, rb, __ffs(mb) - 1);
+        const bool ia = ua && ra == r, ib = ub && rb == r;
+        const int n = (int)__reduce_max_sync(
+            kAll, (uint32_t)max(ia ? pa / kPageSize + 1 : 0, ib ? pb / kPageSize + 1 : 0));
+        emit(nr, r, n);
+        ua = ua && !ia;
+        ub = ub && !ib;
+        ++nr;
+    }
+    return nr;
 }
 
 // S_h = Q_h K^T for the block of npg pages in the ring stage at `kst`, into
@@ -186,28 +219,18 @@ __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p,
         if (u >= c.nunits || *c.abort_flag) break;
         const int g = u % p.kv_heads;
         __syncthreads();  // (2)
-        {  // runs: one per table row among the valid tokens, in order of first token;
-           // lane l holds tokens l and l + 32
-            const int pa = c.sPos[lane], pb = c.sPos[lane + 32];
-            const int ra = c.sRow[lane], rb = c.sRow[lane + 32];
-            bool ua = pa >= 0, ub = pb >= 0;  // valid tokens not yet in a run
-            int nr = 0;
-            for (;;) {
-                const uint32_t ma = __ballot_sync(kAll, ua), mb = __ballot_sync(kAll, ub);
-                if (!ma && !mb) break;
-                const int r = ma ? __shfl_sync(kAll, ra, __ffs(ma) - 1) : __shfl_sync(kAll, rb, __ffs(mb) - 1);
-                const bool ia = ua && ra == r, ib = ub && rb == r;
-                const int n = (int)__reduce_max_sync(
-                    kAll, (uint32_t)max(ia ? pa / kPageSize + 1 : 0, ib ? pb / kPageSize + 1 : 0));
-                if (lane == 0) {
-                    c.sRunRow[nr] = r;
-                    c.sRunPages[nr] = n;
-                }
-                ua = ua && !ia;
-                ub = ub && !ib;
-                ++nr;
-            }
-            if (lane == 0) *c.sNumRuns = nr;
+        {  // the unit's runs: all of the tile's, or the one its item names
+            int tile, run;
+            item_of(c, p, u, tile, run);
+            const int nr = tile_runs(c.sPos[lane], c.sPos[lane + 32], c.sRow[lane], c.sRow[lane + 32],
+                                     [&](int i, int row, int pages) {
+                                         if (lane == 0 && (run < 0 || i == run)) {
+                                             const int k = run < 0 ? i : 0;
+                                             c.sRunRow[k] = row;
+                                             c.sRunPages[k] = pages;
+                                         }
+                                     });
+            if (lane == 0) *c.sNumRuns = run < 0 ? nr : (run < nr ? 1 : 0);
         }
         __syncthreads();  // (3)
         const int nruns = *c.sNumRuns;
@@ -361,7 +384,9 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
         const int u = *c.sUnit;
         if (u >= c.nunits || *c.abort_flag) break;
         const int g = u % p.kv_heads;
-        const int p0 = tile_of(c, p, u) * kTileTok;
+        int tile, run;
+        item_of(c, p, u, tile, run);
+        const int p0 = tile * kTileTok;
         if (tid < kTileTok) {  // the tile's tokens
             const int t = p0 + tid;
             const int len = t < p.P ? p.tok_len[t] : 0;
@@ -677,24 +702,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     pdl_wait();  // prep_kernel's appends, token table and zeroed unit counter
 
-    // ---- unit order: tiles by decreasing page count, ties in token order
+    // ---- work items: the runs of every tile (a tile with none is one empty item,
+    // so that its skipped tokens still get their zero output), in decreasing order
+    // of pages, ties in token order
     const int ntiles = p.ntiles;
-    c.sorted = ntiles <= kMaxSortTiles;
-    c.nunits = ntiles * p.kv_heads;
+    int* sNItems = c.sUnit + 1;
     if (tid < kHeadDim / 4)
         reinterpret_cast<uint2*>(c.sbase + PfSmem::kW)[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
+    if (tid == 0) *sNItems = 0;
+    __syncthreads();
+    if (ntiles <= kMaxSortTiles) {
+        for (int t = warp; t < ntiles; t += kPfThreads / 32) {
+            int pos2[2], row2[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int tok = t * kTileTok + lane + 32 * i;
+                const int len = tok < p.P ? p.tok_len[tok] : 0;
+                pos2[i] = len - 1;
+                row2[i] = len > 0 ? p.tok_row[tok] : -1;
+            }
+            auto add = [&](int run, int pages) {
+                if (lane == 0) {
+                    const int idx = atomicAdd(sNItems, 1);
+                    if (idx < kMaxSortTiles)
+                        sKey[idx] = ((uint32_t)pages << kKeyPagesShift) |
+                                    ((uint32_t)((kMaxSortTiles - 1) - t) << kKeyTileShift) | (uint32_t)(63 - run);
+                }
+            };
+            const int nr = tile_runs(pos2[0], pos2[1], row2[0], row2[1], [&](int i, int, int pages) { add(i, pages); });
+            if (nr == 0) add(0, 0);
+        }
+    } else if (tid == 0) {
+        *sNItems = kMaxSortTiles + 1;
+    }
+    __syncthreads();
+    const int nitems = *sNItems;
+    c.sorted = nitems <= kMaxSortTiles;
+    c.nunits = (c.sorted ? nitems : ntiles) * p.kv_heads;
     if (c.sorted) {
         int n2 = 1;
-        while (n2 < ntiles) n2 <<= 1;
-        for (int i = tid; i < n2; i += kPfThreads) sKey[i] = 0;
-        __syncthreads();
-        for (int t = tid; t < p.P; t += kPfThreads) {
-            const int len = p.tok_len[t];
-            if (len > 0) atomicMax(&sKey[t / kTileTok], (uint32_t)((len - 1) / kPageSize + 1));
-        }
-        __syncthreads();
-        for (int i = tid; i < ntiles; i += kPfThreads)
-            sKey[i] = (sKey[i] << kSortIdxBits) | (uint32_t)((kMaxSortTiles - 1) - i);
+        while (n2 < nitems) n2 <<= 1;
+        for (int i = nitems + tid; i < n2; i += kPfThreads) sKey[i] = 0;
         __syncthreads();
         for (int k = 2; k <= n2; k <<= 1) {  // bitonic sort, descending
             for (int j = k >> 1; j > 0; j >>= 1) {
