@@ -37,6 +37,14 @@
  *     device: the token is skipped (no write, zero output) and a bit is set
  *     in the pool's sticky error word, read with pkv_check_errors().  No
  *     kernel traps or spins without bound.
+ *   - Optional host pre-check: with the environment variable PKV_CHECK=1,
+ *     pkv_decode, pkv_step and pkv_prefill first synchronise the stream, copy
+ *     the call's positions, rows, slots and table to the host and return
+ *     PKV_EINVAL (nothing enqueued) when two written slots coincide outside
+ *     pool page 0, or when a given prompt slot differs from
+ *     table[rows[p]][positions[p] / page_size] * page_size + positions[p] % page_size.
+ *     Tokens the device checks would skip take no part.  The check is for
+ *     debugging: it synchronises, so it does not belong in a captured graph.
  *   - Every `table` argument may be NULL: the contiguous-row layout of the
  *     pages' non-paged entries (src/attention.linnet decode_rows,
  *     prefill_packed, step_packed), where row b owns the `pages` pool pages

@@ -8,6 +8,7 @@
 // synchronises on the call path.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -234,12 +235,74 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
 
 static bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
+// ---- optional host pre-check (environment variable PKV_CHECK=1) ----------------------------
+static bool check_enabled()
+{
+    const char* e = std::getenv("PKV_CHECK");
+    return e && e[0] == '1' && e[1] == 0;
+}
+
+// Copies the call's token tables to the host (synchronising the stream first)
+// and rejects, with PKV_EINVAL, a call whose written slots are not distinct
+// outside pool page 0 or whose given prompt slots differ from those the table
+// derives.  Tokens the device would skip (position, row or page out of range)
+// take no part: the device checks report them.
+static int host_precheck(const pkv_pool* pool, const StepArgs& a, cudaStream_t s)
+{
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ECUDA;
+    auto fetch = [](const int32_t* src, size_t n, std::vector<int32_t>& dst) {
+        dst.resize(n);
+        return n == 0 || cudaMemcpy(dst.data(), src, n * sizeof(int32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
+    };
+    std::vector<int32_t> pos, prow, slots, steps, table;
+    bool ok = fetch(a.positions, a.P, pos) && fetch(a.prow, a.P, prow) && fetch(a.step_positions, a.steps, steps);
+    if (a.slots) ok = ok && fetch(a.slots, a.P, slots);
+    if (a.table) ok = ok && fetch(a.table, (size_t)a.rows * a.pages, table);
+    if (!ok) return PKV_ECUDA;
+    const int S = pool->cfg.page_size;
+    auto page = [&](int row, int j) -> int64_t {
+        return a.table ? (int64_t)table[(size_t)row * a.pages + j] : (int64_t)row * a.pages + j;
+    };
+    // the slot the table gives token (row, p), or -1 if the device would skip the token
+    auto derive = [&](int row, int p) -> int64_t {
+        if (row < 0 || row >= a.rows || p < 0 || p >= pool->cfg.max_seq || p >= a.pages * S) return -1;
+        for (int j = 0; j <= p / S; ++j) {
+            const int64_t id = page(row, j);
+            if (id < 0 || id >= pool->num_pages) return -1;
+        }
+        return page(row, p / S) * S + p % S;
+    };
+    std::vector<int64_t> written;
+    for (int t = 0; t < a.P; ++t) {
+        const int64_t d = derive(prow[t], pos[t]);
+        if (d < 0) continue;
+        if (a.slots) {
+            if (slots[t] < 0 || slots[t] >= pool->num_slots) continue;
+            if (slots[t] != d) return PKV_EINVAL;
+        }
+        written.push_back(d);
+    }
+    for (int b = 0; b < a.steps; ++b) {
+        if (steps[b] == -1) continue;
+        const int64_t d = derive(b, steps[b]);
+        if (d >= 0) written.push_back(d);
+    }
+    std::sort(written.begin(), written.end());
+    for (size_t i = 1; i < written.size(); ++i)
+        if (written[i] == written[i - 1] && written[i] >= S) return PKV_EINVAL;
+    return PKV_OK;
+}
+
 static int run_step(pkv_pool* pool, const StepArgs& a, size_t ws_bytes, void* stream)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
     // contiguous rows (no table): every row's pages must be in the pool
     if (!a.table && (int64_t)a.rows * a.pages > pool->num_pages) return PKV_ERANGE;
+    if (check_enabled()) {
+        const int rc = host_precheck(pool, a, static_cast<cudaStream_t>(stream));
+        if (rc != PKV_OK) return rc;
+    }
     const Plan plan = make_plan(pool, a.P + a.steps, a.pages);
     if (!a.ws || ws_bytes < plan.total) return PKV_EWORKSPACE;
     return enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));

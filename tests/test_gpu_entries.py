@@ -112,3 +112,44 @@ def test_contiguous_rows_must_fit_the_pool():
     assert torch.equal(K.cpu(), wl.K0) and torch.equal(V.cpu(), wl.V0)
     assert pool.check_errors() == 0
     pool.close()
+
+
+# ------------------------------------------------------------------ optional host pre-check
+
+def test_host_precheck_rejects_bad_slots(monkeypatch):
+    """With PKV_CHECK=1 a call whose given prompt slots disagree with the table,
+    or whose written slots coincide outside page 0, is refused before anything
+    is enqueued; consistent calls run and match the oracle."""
+    monkeypatch.setenv("PKV_CHECK", "1")
+    wl = W.make_step("checked step", prompt_lengths=[70, 5], prompt_starts=[60, 0], decode_lengths=[90, 3, 64],
+                     seed=39, table_pages=3)
+    slots = oracle.page_slots(wl.table.numpy(), wl.prow.numpy(), wl.positions.numpy())
+    compare(wl, run_gpu(wl, explicit_slots=slots), run_oracle(wl), label="checked step")
+
+    dev = torch.device("cuda")
+    K, V = wl.K0.to(dev), wl.V0.to(dev)
+    pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+    q, k, v, qw, kw = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w))
+    pos, prow, sp, tab = (t.to(dev) for t in (wl.positions, wl.prow, wl.step_positions, wl.table))
+    out = torch.zeros_like(q)
+    bad = slots.copy()
+    bad[3] = bad[4]                          # token 3 given token 4's slot: off the table, and a duplicate
+    with pytest.raises(pkv.PkvError) as ei:
+        pool.step(q, k, v, qw, kw, pos, prow, torch.as_tensor(bad, dtype=torch.int32).to(dev), sp, tab, out=out)
+    assert ei.value.code == pkv.PKV_EINVAL
+    # two decode rows writing one slot (row 2 steps at row 0's position through row 0's pages)
+    tab2 = wl.table.clone()
+    tab2[2] = tab2[0]
+    sp2 = wl.step_positions.clone()
+    sp2[2] = sp2[0]
+    with pytest.raises(pkv.PkvError) as ei:
+        pool.step(q, k, v, qw, kw, pos, prow, None, sp2.to(dev), tab2.to(dev), out=out)
+    assert ei.value.code == pkv.PKV_EINVAL
+    torch.cuda.synchronize()
+    assert not out.any()
+    assert torch.equal(K.cpu(), wl.K0) and torch.equal(V.cpu(), wl.V0)
+    # without the check the same call is enqueued (its result is unspecified)
+    monkeypatch.delenv("PKV_CHECK")
+    pool.step(q, k, v, qw, kw, pos, prow, None, sp2.to(dev), tab2.to(dev), out=out)
+    torch.cuda.synchronize()
+    pool.close()
