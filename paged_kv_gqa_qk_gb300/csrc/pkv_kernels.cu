@@ -71,6 +71,28 @@ __device__ __forceinline__ float rotate_exact(float u, float up, float2 hi, floa
 
 // The warp's normed + roped k as 4 bf16 (this lane's elements).
 //   kraw: this lane's 4 raw bf16;  wk: its k_norm weights;
+//   rh/rl: (cos, sin) hi and lo parts of this lane's 4 rotation frequencies
+//   4 (lane % 16) .. 4 (lane % 16) + 3 at the token's position.
+__device__ __forceinline__ uint2 norm_rope_k_regs(uint2 kraw, const float (&wk)[4], const float2 (&rh)[4],
+                                                  const float2 (&rl)[4], float eps, int lane)
+{
+    float x[4];
+    unpack4(kraw, x);
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    const float inv = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+    const float sgn = lane < 16 ? -1.f : 1.f;
+    __nv_bfloat16 r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float u = x[i] * wk[i];
+        const float partner = sgn * __shfl_xor_sync(kFull, u, 16);
+        r[i] = __float2bfloat16_rn(__fmul_rn(rotate_exact(u, partner, rh[i], rl[i]), inv));
+    }
+    return make_uint2(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]));
+}
+
 //   rhi/rlo: (cos, sin) hi and lo parts of the token's position, [64].
 __device__ __forceinline__ uint2 norm_rope_k(uint2 kraw, const float (&wk)[4], const float2* rhi, const float2* rlo,
                                              float eps, int lane)
@@ -118,7 +140,10 @@ struct PrepParams {
     uint32_t* err;
 };
 
-// One CTA (4 warps) per token; warp w appends kv heads w, w+4, ...
+// One CTA (4 warps) per token; warp w appends kv heads w, w+4, ...  Every
+// load that does not depend on another (the table entries, the slot, the
+// token's k and v, the RoPE row, the weights) is issued before the first use,
+// so that the token costs about two memory latencies.
 __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
 {
     const int t = blockIdx.x;
@@ -141,26 +166,49 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
         else if (pos < 0 || pos >= p.max_seq || pos >= p.pages * kPageSize)
             e = PKV_DEVERR_POSITION;
     }
-    // Every page the token will read must be a pool page.
+    const bool inrange = active && !e;
+    // every page the token will read must be a pool page
     int bad = 0;
-    if (active && !e) {
-        const int npg = pos / kPageSize + 1;
-        for (int i = tid; i < npg; i += blockDim.x) {
-            const int id = page_of(p.table, p.pages, row, i);
-            bad |= (id < 0 || id >= p.num_pages);
-        }
+    const int npg = inrange ? pos / kPageSize + 1 : 0;
+    for (int i = tid; i < npg; i += blockDim.x) {
+        const int id = page_of(p.table, p.pages, row, i);
+        bad |= (id < 0 || id >= p.num_pages);
     }
-    bad = __syncthreads_or(bad);
-    if (active && !e && bad) e = PKV_DEVERR_PAGE;
     int64_t slot = 0;
-    if (active && !e) {
-        if (t < p.P && p.slots) {
+    if (inrange) {
+        if (t < p.P && p.slots)
             slot = p.slots[t];
-            if (slot < 0 || slot >= p.num_slots) e = PKV_DEVERR_SLOT;
-        } else {
+        else
             slot = (int64_t)page_of(p.table, p.pages, row, pos / kPageSize) * kPageSize + pos % kPageSize;
+    }
+    // the token's k and v for this warp's first two kv heads, its RoPE row, the weights
+    const int pc = inrange ? pos : 0;
+    uint2 kraw[2] = {}, vraw[2] = {};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int g = warp + 4 * i;
+        if (g < p.kv_heads) {
+            const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim + 4 * lane;
+            kraw[i] = *reinterpret_cast<const uint2*>(p.k + src);
+            vraw[i] = *reinterpret_cast<const uint2*>(p.v + src);
         }
     }
+    float2 rh[4], rl[4];
+    {
+        const float4* h4 = reinterpret_cast<const float4*>(p.rope_hi + (int64_t)pc * kRopeHalf + 4 * (lane & 15));
+        const float4* l4 = reinterpret_cast<const float4*>(p.rope_lo + (int64_t)pc * kRopeHalf + 4 * (lane & 15));
+        const float4 a = h4[0], b = h4[1], c = l4[0], d = l4[1];
+        rh[0] = make_float2(a.x, a.y), rh[1] = make_float2(a.z, a.w), rh[2] = make_float2(b.x, b.y),
+        rh[3] = make_float2(b.z, b.w);
+        rl[0] = make_float2(c.x, c.y), rl[1] = make_float2(c.z, c.w), rl[2] = make_float2(d.x, d.y),
+        rl[3] = make_float2(d.z, d.w);
+    }
+    float wk[4];
+    unpack4(*reinterpret_cast<const uint2*>(p.kw + 4 * lane), wk);
+
+    bad = __syncthreads_or(bad);
+    if (inrange && bad) e = PKV_DEVERR_PAGE;
+    if (inrange && !e && t < p.P && p.slots && (slot < 0 || slot >= p.num_slots)) e = PKV_DEVERR_SLOT;
     if (tid == 0) {
         if (t == 0) *p.sched = 0;
         const bool ok = active && !e;
@@ -170,17 +218,19 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
     }
     if (!active || e) return;
 
-    float wk[4];
-    unpack4(*reinterpret_cast<const uint2*>(p.kw + 4 * lane), wk);
-    const float2* rhi = p.rope_hi + (int64_t)pos * kRopeHalf;
-    const float2* rlo = p.rope_lo + (int64_t)pos * kRopeHalf;
-    for (int g = warp; g < p.kv_heads; g += 4) {
-        const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim;
-        const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim;
-        const uint2 kraw = *reinterpret_cast<const uint2*>(p.k + src + 4 * lane);
-        const uint2 vraw = *reinterpret_cast<const uint2*>(p.v + src + 4 * lane);
-        *reinterpret_cast<uint2*>(p.K + dst + 4 * lane) = norm_rope_k(kraw, wk, rhi, rlo, p.eps, lane);
-        *reinterpret_cast<uint2*>(p.V + dst + 4 * lane) = vraw;  // v is written as given
+    for (int g = warp, i = 0; g < p.kv_heads; g += 4, ++i) {
+        const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane;
+        uint2 kr, vr;
+        if (i < 2) {
+            kr = kraw[i & 1];
+            vr = vraw[i & 1];
+        } else {
+            const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim + 4 * lane;
+            kr = *reinterpret_cast<const uint2*>(p.k + src);
+            vr = *reinterpret_cast<const uint2*>(p.v + src);
+        }
+        *reinterpret_cast<uint2*>(p.K + dst) = norm_rope_k_regs(kr, wk, rh, rl, p.eps, lane);
+        *reinterpret_cast<uint2*>(p.V + dst) = vr;  // v is written as given
     }
 }
 
