@@ -9,7 +9,7 @@ implies), with the attention kernel's achieved HBM bandwidth against the
 measured copy bandwidth of the chip.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload config2|config3|config4|config5|sweepRxL|prefill|rows]
+                  [--workload config2|config3|config4|config5|sweepRxL|prefill|rows|linear_decode|linear_prefill]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch of the
@@ -422,6 +422,142 @@ def run_gpu(args) -> None:
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------- the projections (pkv_linear)
+
+LINEAR_SHAPES = (("q_proj", 4096, 4096), ("k_proj", 1024, 4096), ("v_proj", 1024, 4096), ("o_proj", 4096, 4096))
+
+
+def run_gpu_linear(args) -> None:
+    """The four projections around one attention layer (q/k/v before it, o_proj
+    after it) for `tokens` tokens: 64 (the decode batch) or 2048 (the prompts of
+    the step workload).  One step = four pkv_linear calls."""
+    import torch
+    import paged_kv_gqa_qk_gb300 as pkv
+    import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    pkv.load_library()
+    tokens = {"linear_decode": 64, "linear_prefill": 2048}[args.workload]
+    pool = pkv.PagedKVPool(torch.zeros(8, 64, 128, dtype=torch.bfloat16, device=dev),
+                           torch.zeros(8, 64, 128, dtype=torch.bfloat16, device=dev))
+    host_x, _ = W.make_linear(tokens, 4096, 128, seed=rank_seed(3000 + tokens, rank))
+    host_a, _ = W.make_linear(tokens, 4096, 128, seed=rank_seed(3001 + tokens, rank))  # the attention output
+    ws = [W.make_linear(1, i, o, seed=rank_seed(3100 + j, rank))[1].to(dev) for j, (_, o, i) in enumerate(LINEAR_SHAPES)]
+    x, a = host_x.to(dev), host_a.to(dev)
+    ys = [torch.empty(tokens, o, dtype=torch.bfloat16, device=dev) for _, o, _ in LINEAR_SHAPES]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for j in range(4):
+            pool.linear(a if j == 3 else x, ws[j], ys[j], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)  # the weights (84 MB) fit in L2
+
+    def flush():
+        with torch.cuda.stream(stream):
+            flush_buf.zero_()
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush()
+            evs[2 * i].record(stream)
+            step()
+            evs[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        pkv.pkv_timer_enable(pool.handle, True)
+        for _ in range(args.steps):
+            flush()
+            step()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)), world) / args.steps
+    k_ms, k_n = pkv.pkv_timer_read(pool.handle)
+    pkv.pkv_timer_enable(pool.handle, False)
+
+    host_in = [host_x.pin_memory(), host_a.pin_memory()]
+    host_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            flush()
+            x.copy_(host_in[0], non_blocking=True)
+            a.copy_(host_in[1], non_blocking=True)
+            step()
+            for h, y in zip(host_out, ys):
+                h.copy_(y, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    flags = pkv.pkv_check_errors(pool.handle, stream)
+    if flags:
+        raise SystemExit(f"device error flags {flags}")
+
+    weight_bytes = sum(2 * o * i for _, o, i in LINEAR_SHAPES)
+    act_bytes = sum(2 * tokens * (i + o) for _, o, i in LINEAR_SHAPES)
+    flops = sum(2 * tokens * o * i for _, o, i in LINEAR_SHAPES)
+    kern_s = k_ms / 1e3 / max(k_n, 1) * 4  # the four launches of one step
+    timing = "CUDA events around each matrix-product launch (four per step), second timed pass"
+    if tokens <= 256:   # weight streaming: bound by HBM
+        peak, peak_kind = measured_peak_hbm()
+        roofline = {"bound": "hbm", "kernel": "linear_kernel", "achieved": (weight_bytes + act_bytes) / kern_s / 1e9,
+                    "peak": peak, "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s",
+                    "algorithmic_bytes_per_step": weight_bytes + act_bytes}
+    else:
+        peak, peak_kind = measured_peak_bf16()
+        roofline = {"bound": "tensor", "kernel": "linear_kernel", "achieved": flops / kern_s / 1e12,
+                    "peak": peak, "peak_kind": f"{peak_kind} (dense bf16 TFLOP/s, burst)", "unit": "TFLOP/s",
+                    "algorithmic_flops_per_step": flops}
+    roofline.update({"frac": roofline["achieved"] / peak, "traffic": None,
+                     "avg_launch_us": k_ms * 1e3 / max(k_n, 1), "timed_launches": k_n, "timing": timing})
+    res = {
+        "metric": METRIC,
+        "value": tokens * world / (ms_step / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,1/4096) bf16 weights)",
+        "config": {"workload": f"projections q/k/v/o of one layer, {tokens} tokens, hidden 4096",
+                   "tokens": tokens, "shapes": [list(s) for s in LINEAR_SHAPES],
+                   "l2": f"L2 flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the "
+                         f"device-timed events, inside the e2e time): {weight_bytes / 1e6:.0f} MB of weights",
+                   "parallelism": f"dp{world} (independent replicas)"},
+        "roofline": roofline,
+        "e2e": {"value": tokens * args.steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(1 + (pkv.pkv_linear_workspace_bytes(pool.handle, tokens, i, o) > 0)
+                            for _, o, i in LINEAR_SHAPES) * args.steps,
+        "clocks": clk.summary(),
+    }
+    pool.close()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------------------- the oracle (CPU)
 
 def _oracle_step(wl, rows, K, V, args_bits, nthreads):
@@ -521,6 +657,8 @@ def main(argv=None):
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload.startswith("linear"):
+        run_gpu_linear(args)
     else:
         run_gpu(args)
 

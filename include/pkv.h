@@ -251,6 +251,28 @@ PKV_API int pkv_prefill(pkv_pool* pool, const void* q, const void* k, const void
                         const int32_t* table, int P, int rows, int pages, void* out, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* ---- the projections either side: linear layers -------------------------------------
+ * qwen3-8b Nest files, src/attention.linnet GroupedQueryAttention.decode_paged and
+ * step_paged: q_proj, k_proj and v_proj map the layer input x [tokens][hidden] to
+ * q [tokens][heads * head_dim] and k, v [tokens][kv_heads * head_dim] (split_heads
+ * of these is the [tokens][heads][head_dim] layout pkv_decode / pkv_step take, a
+ * reshape), and o_proj maps merge_heads of their output back to [tokens][hidden].
+ * None has a bias (README.md).  One call computes one of them:
+ *   y[t][o] = sum_k x[t][k] * w[o][k]   (bf16 inputs, fp32 accumulation, bf16 output)
+ *
+ *   x          device bf16 [tokens][in_features], in_features % 64 == 0, 16-byte aligned
+ *   w          device bf16 [out_features][in_features] (nn.Linear layout), out_features % 128 == 0
+ *   y          device bf16 [tokens][out_features], 16-byte aligned
+ *   workspace  device, >= pkv_linear_workspace_bytes(...), 256-byte aligned; 0 bytes when
+ *              the output tiles alone fill the GPU, else fp32 partial sums of the input
+ *              features split over several CTAs (few tokens: the decode step)
+ * The pool names the device and receives device errors; nothing of it is read.
+ * Other feature counts return PKV_ENOTIMPL; returns once the work is enqueued. */
+PKV_API int pkv_linear_workspace_bytes(const pkv_pool* pool, int tokens, int in_features, int out_features,
+                                       size_t* bytes);
+PKV_API int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in_features,
+                       int out_features, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- decode without a caller workspace -------------------------------------------------------
  * The pages have no counterpart to this entry point; it is a convenience of
  * this library.  It is pkv_decode for callers that cannot allocate device
@@ -294,7 +316,8 @@ PKV_API int pkv_set_ctas(pkv_pool* pool, int ctas);
 
 /* Kernel timer: while enabled, every pkv_decode / pkv_step records a pair of
  * CUDA events on its stream around the decode attention kernel (the dominant
- * launch), and every pkv_prefill around its prompt-attention kernel.  pkv_timer_read synchronises on the last recorded event,
+ * launch), every pkv_prefill around its prompt-attention kernel and every
+ * pkv_linear around its matrix-product kernel.  pkv_timer_read synchronises on the last recorded event,
  * returns the summed duration in milliseconds and the number of timed
  * launches since the timer was last enabled, and keeps the timer running.
  * At most 4096 launches are kept (later ones overwrite the oldest). */

@@ -248,3 +248,10 @@ def decode(K, V, q, k, v, q_norm_w, k_norm_w, positions, table, cfg: dict | None
     """``decode_paged``: step with no prompt tokens. Returns (out [R][heads][D] float64, err_bits)."""
     return step(K, V, q, k, v, q_norm_w, k_norm_w, None, None, None, positions, table, cfg=cfg, sel=sel,
                 nthreads=nthreads)
+
+
+def linear(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """A projection without bias, y[t][o] = sum_k x[t][k] w[o][k] (qwen3-8b Nest files,
+    src/attention.linnet: q_proj / k_proj / v_proj / o_proj), in float64 on the exact
+    values of bf16 x [tokens][in] and w [out][in]; a library matrix product is the step."""
+    return bf16_to_f64(_u16(x_bits)) @ bf16_to_f64(_u16(w_bits)).T

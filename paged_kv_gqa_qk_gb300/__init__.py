@@ -26,7 +26,8 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 # Every symbol include/pkv.h declares.
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
                "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_prefill", "pkv_check_errors",
-               "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static")
+               "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static",
+               "pkv_linear_workspace_bytes", "pkv_linear")
 
 # Size of the scratch array pkv_decode_static uses in place of a workspace.
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_timer_enable": ([vp, i32], i32),
         "pkv_timer_read": ([vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)], i32),
         "pkv_decode_static": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp], i32),
+        "pkv_linear_workspace_bytes": ([vp, i32, i32, i32, ctypes.POINTER(sz)], i32),
+        "pkv_linear": ([vp, vp, vp, vp, i32, i32, i32, vp, sz, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -231,6 +234,24 @@ def pkv_prefill(pool, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, table
         _stream(stream)), "pkv_prefill")
 
 
+def pkv_linear_workspace_bytes(pool, tokens: int, in_features: int, out_features: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().pkv_linear_workspace_bytes(pool, int(tokens), int(in_features), int(out_features),
+                                                      ctypes.byref(n)), "pkv_linear_workspace_bytes")
+    return n.value
+
+
+def pkv_linear(pool, x, w, y, workspace=None, stream=None) -> None:
+    """y = x w^T: x [tokens][in], w [out][in] (nn.Linear layout), y [tokens][out], all bf16."""
+    if x.dim() != 2 or w.dim() != 2 or y.dim() != 2 or x.shape[1] != w.shape[1] or y.shape != (x.shape[0], w.shape[0]):
+        raise ValueError(f"shapes x {tuple(x.shape)}, w {tuple(w.shape)}, y {tuple(y.shape)} do not match y = x w^T")
+    ws = ctypes.c_void_p(None) if workspace is None else _dev(workspace, torch.uint8, "workspace")
+    _check(load_library().pkv_linear(
+        pool, _dev(x, torch.bfloat16, "x"), _dev(w, torch.bfloat16, "w"), _dev(y, torch.bfloat16, "y"),
+        int(x.shape[0]), int(x.shape[1]), int(w.shape[0]), ws, 0 if workspace is None else workspace.numel(),
+        _stream(stream)), "pkv_linear")
+
+
 def pkv_check_errors(pool, stream=None) -> int:
     f = ctypes.c_uint32()
     _check(load_library().pkv_check_errors(pool, _stream(stream), ctypes.byref(f)), "pkv_check_errors")
@@ -265,6 +286,7 @@ class PagedKVPool:
         self.num_pages = K.shape[1] // c.page_size
         self.handle = pkv_pool_wrap(c, self.num_pages, K, V, stream)
         self._ws = None
+        self._lws = None
 
     def workspace(self, rows: int, pages: int, prefill_tokens: int = 0) -> torch.Tensor:
         n = pkv_workspace_bytes(self.handle, rows, pages, prefill_tokens)
@@ -300,6 +322,19 @@ class PagedKVPool:
         pkv_prefill(self.handle, q, k, v, q_norm_w, k_norm_w, positions, prow, slots, table, out, ws, stream,
                     rows=rows, pages=pages)
         return out
+
+    def linear(self, x, w, y=None, stream=None) -> torch.Tensor:
+        """y = x w^T on this pool's device (a projection before or after the attention)."""
+        if y is None:
+            y = torch.empty(x.shape[0], w.shape[0], dtype=torch.bfloat16, device=x.device)
+        n = pkv_linear_workspace_bytes(self.handle, x.shape[0], x.shape[1], w.shape[0])
+        ws = None
+        if n:
+            if self._lws is None or self._lws.numel() < n:
+                self._lws = torch.empty(n, dtype=torch.uint8, device=x.device)
+            ws = self._lws
+        pkv_linear(self.handle, x, w, y, ws, stream)
+        return y
 
     def check_errors(self, stream=None) -> int:
         return pkv_check_errors(self.handle, stream)

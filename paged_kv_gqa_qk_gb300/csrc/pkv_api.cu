@@ -128,6 +128,24 @@ static bool make_tmap(CUtensorMap* map, void* base, int64_t num_slots, int kv_he
     return r == CUDA_SUCCESS;
 }
 
+// 2-D tiled view {inner, outer} of a row-major bf16 matrix with `row_bytes`
+// between rows; a box is box_inner x box_outer elements with 128-byte swizzle,
+// and reads past the matrix's edge fill zeros.
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static int check_config(const pkv_config* c)
 {
     if (c->heads <= 0 || c->kv_heads <= 0 || c->head_dim <= 0 || c->page_size <= 0 || c->max_seq <= 0)
@@ -449,6 +467,34 @@ int pkv_prefill(pkv_pool* pool, const void* q, const void* k, const void* v, con
     StepArgs a = {q, k, v, q_norm_w, k_norm_w, positions, prow, slots, nullptr, table,
                   P, rows, pages, 0, out, static_cast<char*>(workspace)};
     return run_step(pool, a, workspace_bytes, stream);
+}
+
+int pkv_linear_workspace_bytes(const pkv_pool* pool, int tokens, int in_features, int out_features, size_t* bytes)
+{
+    if (!pool || !bytes || tokens <= 0 || in_features <= 0 || out_features <= 0) return PKV_EINVAL;
+    if (in_features % 64 || out_features % 128) return PKV_ENOTIMPL;
+    if ((int64_t)tokens * out_features > ((int64_t)1 << 34) / 4) return PKV_ERANGE;
+    const int splits = linear_splits(pool, tokens, in_features, out_features);
+    *bytes = splits > 1 ? (size_t)splits * tokens * out_features * sizeof(float) : 0;
+    return PKV_OK;
+}
+
+int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in_features, int out_features,
+               void* workspace, size_t workspace_bytes, void* stream)
+{
+    size_t need = 0;
+    if (!pool || !x || !w || !y) return PKV_EINVAL;
+    const int rc = pkv_linear_workspace_bytes(pool, tokens, in_features, out_features, &need);
+    if (rc != PKV_OK) return rc;
+    if (tokens > (1 << 24) || out_features > (1 << 20) || in_features > (1 << 20)) return PKV_ERANGE;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16)) return PKV_EINVAL;
+    if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_EWORKSPACE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    return launch_linear(pool, x, w, y, tokens, in_features, out_features, workspace,
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ECUDA;
 }
 
 int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags)

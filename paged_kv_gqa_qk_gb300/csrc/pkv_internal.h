@@ -85,6 +85,18 @@ __device__ __forceinline__ int page_of(const int32_t* table, int pages, int row,
     return table ? table[(int64_t)row * pages + j] : row * pages + j;
 }
 
+// 2-D tiled tensor map of a row-major bf16 matrix (128-byte swizzle, zero fill
+// past the edges); false if the driver refuses it.
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer);
+
+// y = x W^T (pkv_linear): tokens per tile, input-feature splits, and the launch
+// (the fp32 partials go to `part` when there is more than one split).
+int linear_tile_tokens(int tokens);
+int linear_splits(const pkv_pool* pool, int tokens, int in, int out);
+cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in, int out,
+                          void* part, cudaStream_t s);
+
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.
 cudaError_t configure_kernels();

@@ -58,7 +58,9 @@ def test_null_arguments_are_rejected(lib):
     assert lib.pkv_decode(None, *([None] * 7), 1, 1, None, None, 0, None) == pkv.PKV_EINVAL
     assert lib.pkv_step(None, *([None] * 10), 1, 1, 1, None, None, 0, None) == pkv.PKV_EINVAL
     assert lib.pkv_prefill(None, *([None] * 9), 1, 1, 1, None, None, 0, None) == pkv.PKV_EINVAL
+    assert lib.pkv_linear(None, None, None, None, 1, 64, 128, None, 0, None) == pkv.PKV_EINVAL
     n = ctypes.c_size_t()
+    assert lib.pkv_linear_workspace_bytes(None, 1, 64, 128, ctypes.byref(n)) == pkv.PKV_EINVAL
     assert lib.pkv_workspace_bytes(None, 1, 1, 0, ctypes.byref(n)) == pkv.PKV_EINVAL
     assert lib.pkv_pool_free(None) == pkv.PKV_OK
     assert lib.pkv_pool_kv(None, None, None, None) == pkv.PKV_EINVAL

@@ -338,6 +338,31 @@ def test_prefill_over_contiguous_rows_equals_packed_attention():
     assert not out[P:].any()   # the table rows take no step
 
 
+# ------------------------------------------------------------------ projections (linear, no bias)
+
+def test_linear_brute_force_and_special_cases():
+    """y[t][o] = sum_k x[t][k] w[o][k]: pure-Python sums on tiny shapes, the
+    identity weight returns x, a one-hot input row returns a column of w, and
+    the map is linear in x."""
+    rng = np.random.default_rng(11)
+    x, w = rand_bits(rng, (3, 7)), rand_bits(rng, (5, 7))
+    y = oracle.linear(x, w)
+    xf, wf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(w)
+    for t in range(3):
+        for o in range(5):
+            ref = 0.0
+            for k in range(7):
+                ref += float(xf[t, k]) * float(wf[o, k])
+            assert abs(y[t, o] - ref) <= 1e-12 * max(1.0, abs(ref))
+    eye = W.bits(torch.eye(7, dtype=torch.bfloat16))
+    np.testing.assert_array_equal(oracle.linear(x, eye), xf)
+    onehot = np.zeros((1, 7), np.uint16)
+    onehot[0, 4] = W.bits(torch.ones(1, dtype=torch.bfloat16))[0]
+    np.testing.assert_array_equal(oracle.linear(onehot, w)[0], wf[:, 4])
+    # linear in x: two inputs whose exact sum is again a bf16 value (x and x itself)
+    np.testing.assert_array_equal(oracle.linear(W.bits(torch.from_numpy(2 * xf).to(torch.bfloat16)), w), 2 * y)
+
+
 # ------------------------------------------------------------------ a7 prefill chunk == sequential decode
 
 def test_step_prefill_equals_sequential_decode():

@@ -343,3 +343,13 @@ def sweep(rows: int, length: int, seed: int | None = None) -> Workload:
     s = seed if seed is not None else 2000 + rows + length
     return make_decode(f"decode {rows} rows x {length}", [length] * rows, seed=s,
                        table_pages=_pages_for(length, DEFAULT_CONFIG["page_size"]))
+
+
+def make_linear(tokens: int, in_features: int, out_features: int, seed: int):
+    """x [tokens][in] ~ N(0,1) and w [out][in] ~ N(0, 1/in), both rounded to bf16
+    (outputs of order 1, as a projection of a normed hidden state gives)."""
+    gen = torch.Generator().manual_seed(seed)
+    x = _randn_bf16(gen, (tokens, in_features))
+    w = (torch.randn(out_features, in_features, generator=gen, dtype=torch.float32) / in_features ** 0.5).to(
+        torch.bfloat16)
+    return x, w
