@@ -263,9 +263,10 @@ PKV_API int pkv_prefill(pkv_pool* pool, const void* q, const void* k, const void
  *   x          device bf16 [tokens][in_features], in_features % 64 == 0, 16-byte aligned
  *   w          device bf16 [out_features][in_features] (nn.Linear layout), out_features % 128 == 0
  *   y          device bf16 [tokens][out_features], 16-byte aligned
- *   workspace  device, >= pkv_linear_workspace_bytes(...), 256-byte aligned; 0 bytes when
- *              the output tiles alone fill the GPU, else fp32 partial sums of the input
- *              features split over several CTAs (few tokens: the decode step)
+ *   workspace  device, >= pkv_linear_workspace_bytes(...), 256-byte aligned: 0 bytes in
+ *              this version (may be NULL): when few tokens leave SMs idle, the input
+ *              features are split over the CTAs of a cluster, which sum their fp32
+ *              partial tiles in shared memory
  * The pool names the device and receives device errors; nothing of it is read.
  * Other feature counts return PKV_ENOTIMPL; returns once the work is enqueued. */
 PKV_API int pkv_linear_workspace_bytes(const pkv_pool* pool, int tokens, int in_features, int out_features,

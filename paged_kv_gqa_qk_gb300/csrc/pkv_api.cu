@@ -474,8 +474,7 @@ int pkv_linear_workspace_bytes(const pkv_pool* pool, int tokens, int in_features
     if (!pool || !bytes || tokens <= 0 || in_features <= 0 || out_features <= 0) return PKV_EINVAL;
     if (in_features % 64 || out_features % 128) return PKV_ENOTIMPL;
     if ((int64_t)tokens * out_features > ((int64_t)1 << 34) / 4) return PKV_ERANGE;
-    const int splits = linear_splits(pool, tokens, in_features, out_features);
-    *bytes = splits > 1 ? (size_t)splits * tokens * out_features * sizeof(float) : 0;
+    *bytes = 0;  // split sums stay in the cluster's shared memory
     return PKV_OK;
 }
 
@@ -491,8 +490,8 @@ int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens
     if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_EWORKSPACE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
-    return launch_linear(pool, x, w, y, tokens, in_features, out_features, workspace,
-                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+    return launch_linear(pool, x, w, y, tokens, in_features, out_features, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
                ? PKV_OK
                : PKV_ECUDA;
 }

@@ -90,12 +90,12 @@ __device__ __forceinline__ int page_of(const int32_t* table, int pages, int row,
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                   uint32_t box_inner, uint32_t box_outer);
 
-// y = x W^T (pkv_linear): tokens per tile, input-feature splits, and the launch
-// (the fp32 partials go to `part` when there is more than one split).
+// y = x W^T (pkv_linear): tokens per tile, input-feature splits (CTAs of one
+// cluster), and the launch.
 int linear_tile_tokens(int tokens);
 int linear_splits(const pkv_pool* pool, int tokens, int in, int out);
 cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in, int out,
-                          void* part, cudaStream_t s);
+                          cudaStream_t s);
 
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.

@@ -16,8 +16,10 @@
 // warps read the accumulator back and write y (lanes of a warp write 32
 // consecutive output features of one token: 64 contiguous bytes).  When the
 // tiles alone would leave most SMs idle (few tokens: the decode step), the
-// input features are split over `splits` CTAs that write fp32 partial tiles
-// to the workspace, and a second kernel sums them in a fixed order.
+// input features are split over the `splits` CTAs of a thread-block cluster:
+// each stages its fp32 partial tile in its own shared memory, and CTA r of the
+// cluster sums slice r of the features over all of them (distributed shared
+// memory, in a fixed order) and writes it.
 #include <cuda_bf16.h>
 
 #include "pkv_internal.h"
@@ -30,28 +32,29 @@ namespace {
 constexpr int kLinThreads = 128;
 constexpr int kBM = 128;         // output features per tile (M)
 constexpr int kBK = 64;          // input features per ring stage (one 128-byte swizzle span)
-constexpr int kLinSmem = 192 * 1024;
+constexpr int kMaxSplits = 8;    // a portable cluster
 
 template <int BN>
 struct LinShape {
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KiB of W
     static constexpr int kBBytes = BN * kBK * 2;   // x
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = kLinSmem / kStageBytes;
+    // 64-token tiles (the decode step) keep two CTAs per SM resident: 96 KiB rings
+    static constexpr int kStages = BN == 64 ? 4 : (192 * 1024) / kStageBytes;
+    static_assert(kStages * kStageBytes >= kBM * BN * 4, "the ring holds the fp32 partial tile");
     static constexpr int kBars = kStages * kStageBytes;  // full[S], empty[S], done
     static constexpr int kTmemSlot = kBars + 8 * (2 * kStages + 1);
     static constexpr int kAlloc = kTmemSlot + 16 + 1024;
 };
 
 struct LinParams {
-    __nv_bfloat16* y;   // [tokens][out], when splits == 1
-    float* part;        // [splits][tokens][out], when splits > 1
+    __nv_bfloat16* y;   // [tokens][out]
     uint32_t* err;
     int tokens, in, out, splits;
 };
 
 template <int BN>
-__global__ void __launch_bounds__(kLinThreads, 1)
+__global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
     linear_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, LinParams p)
 {
     using S = LinShape<BN>;
@@ -81,13 +84,25 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + S::kTmemSlot);
 
+    pdl_launch_dependents();  // the next projection may start streaming its weights
     if (warp == 0 && lane == 0) {
-        // ---- producer: the W box (128 features x 64 inputs) and the x box (BN tokens x 64 inputs)
+        // ---- producer: the W box (128 features x 64 inputs) and the x box (BN tokens x 64 inputs).
+        // The first stages' weights are requested before waiting for the kernel before this one
+        // (which may still be writing x); nothing this kernel writes is touched before the wait.
         const uint64_t pol_w = l2_policy_evict_first();  // each weight tile is read by one CTA per token tile
         const uint64_t pol_x = l2_policy_evict_last();   // x is read by every output tile
-        for (int k = k0; k < k1; ++k) {
+        const int early = min(k1 - k0, S::kStages);
+        for (int i = 0; i < early; ++i) {
+            const uint32_t a = base + i * S::kStageBytes, fb = bar_full + 8 * i;
+            mbar_arrive_expect_tx(fb, S::kStageBytes);
+            tma_load_2d(a, &tmW, (k0 + i) * kBK, m0, fb, pol_w);
+        }
+        pdl_wait();
+        for (int i = 0; i < early; ++i)
+            tma_load_2d(base + i * S::kStageBytes + S::kABytes, &tmX, (k0 + i) * kBK, n0, bar_full + 8 * i, pol_x);
+        for (int k = k0 + early; k < k1; ++k) {
             const int i = k - k0, st = i % S::kStages;
-            if (i >= S::kStages && !mbar_wait(bar_empty + 8 * st, ((i / S::kStages) - 1) & 1)) {
+            if (!mbar_wait(bar_empty + 8 * st, ((i / S::kStages) - 1) & 1)) {
                 atomicOr(p.err, PKV_DEVERR_TIMEOUT);
                 break;
             }
@@ -118,58 +133,74 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     __syncwarp();
 
     // ---- epilogue: thread (warp w, lane l) holds output feature m0 + 32 w + l for BN tokens
+    pdl_wait();  // y may be read by the kernel before this one
     const bool ok = mbar_wait(bar_done, 0);
     tc_fence_after();
     const int o = m0 + 32 * warp + lane;
-    if (ok && k1 > k0) {
+    if (p.splits == 1) {
+        if (ok) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
-            tmem_wait_ld_regs(v);
-            if (p.splits == 1) {
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
+                tmem_wait_ld_regs(v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = n0 + c0 + j;
                     if (t < p.tokens) p.y[(int64_t)t * p.out + o] = __float2bfloat16_rn(__uint_as_float(v[j]));
                 }
-            } else {
-                float* dst = p.part + (int64_t)split * p.tokens * p.out;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = n0 + c0 + j;
-                    if (t < p.tokens) dst[(int64_t)t * p.out + o] = __uint_as_float(v[j]);
-                }
             }
         }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, BN);
+        }
+        return;
+    }
+    // ---- split over the cluster: the partial tile, [token][feature] fp32, in this CTA's idle ring
+    float* part = reinterpret_cast<float*>(sbase);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
+        tmem_wait_ld_regs(v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) part[(c0 + j) * kBM + 32 * warp + lane] = ok ? __uint_as_float(v[j]) : 0.f;
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // every partial tile of the cluster is in place
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, BN);
     }
-}
-
-// y = bf16 of the sum of the split partials, in split order.
-__global__ void __launch_bounds__(256) linear_reduce_kernel(LinParams p)
-{
-    const int64_t n4 = (int64_t)p.tokens * p.out / 4;
-    const int64_t stride = (int64_t)p.tokens * p.out / 4;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-        float4 acc = reinterpret_cast<const float4*>(p.part)[i];
-        for (int s = 1; s < p.splits; ++s) {
-            const float4 b = reinterpret_cast<const float4*>(p.part)[s * stride + i];
-            acc.x += b.x;
-            acc.y += b.y;
-            acc.z += b.z;
-            acc.w += b.w;
+    // CTA r sums features [r * 128 / ns, (r + 1) * 128 / ns) of the tile over the ns CTAs, in
+    // rank order, four features (16 bytes) at a time
+    const int ns = p.splits, per4 = kBM / ns / 4, r = (int)cluster_rank();
+    const uint32_t local = smem_u32(part);
+    for (int idx = tid; idx < BN * per4; idx += kLinThreads) {
+        const int t = idx / per4, f = r * (kBM / ns) + 4 * (idx % per4);
+        const uint32_t off = (uint32_t)(t * kBM + f) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kMaxSplits; ++q) {
+            if (q < ns) {
+                const float4 v = ld_cluster_f32x4(cluster_map(local + off, q));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
         }
-        uint2 r;
-        r.x = pack_bf16(__float2bfloat16_rn(acc.x), __float2bfloat16_rn(acc.y));
-        r.y = pack_bf16(__float2bfloat16_rn(acc.z), __float2bfloat16_rn(acc.w));
-        reinterpret_cast<uint2*>(p.y)[i] = r;
+        if (n0 + t < p.tokens) {
+            uint2 o2;
+            o2.x = pack_bf16(__float2bfloat16_rn(acc.x), __float2bfloat16_rn(acc.y));
+            o2.y = pack_bf16(__float2bfloat16_rn(acc.z), __float2bfloat16_rn(acc.w));
+            *reinterpret_cast<uint2*>(p.y + (int64_t)(n0 + t) * p.out + m0 + f) = o2;
+        }
     }
+    cluster_sync();  // no CTA leaves while another reads its shared memory
 }
 
 template <int BN>
@@ -183,45 +214,54 @@ cudaError_t launch_linear_bn(pkv_pool* pool, const void* x, const void* w, const
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(linear_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
     if (e != cudaSuccess) return e;
-    const dim3 grid(p.out / kBM, (p.tokens + BN - 1) / BN, splits);
     const bool timed = pool->timer_on;
     const int slot = (int)(pool->timer_count % kTimerSlots);
     if (timed && (e = cudaEventRecord(pool->ev_start[slot], s)) != cudaSuccess) return e;
-    linear_kernel<BN><<<grid, kLinThreads, S::kAlloc, s>>>(tmW, tmX, p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.out / kBM, (p.tokens + BN - 1) / BN, splits);
+    cfg.blockDim = dim3(kLinThreads);
+    cfg.dynamicSmemBytes = S::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = timed ? 0 : 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, linear_kernel<BN>, tmW, tmX, p);
     if (e != cudaSuccess) return e;
     if (timed) {
         if ((e = cudaEventRecord(pool->ev_stop[slot], s)) != cudaSuccess) return e;
         pool->timer_count++;
     }
-    if (splits == 1) return cudaSuccess;
-    const int64_t n4 = (int64_t)p.tokens * p.out / 4;
-    const int blocks = (int)((n4 + 255) / 256 < 4 * pool->num_sms ? (n4 + 255) / 256 : 4 * pool->num_sms);
-    linear_reduce_kernel<<<blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace
 
 int linear_tile_tokens(int tokens) { return tokens <= 64 ? 64 : tokens <= 128 ? 128 : 256; }
 
-// Split the input features over CTAs only while the output tiles alone fill
-// less than half the SMs, and keep at least 4 steps of 64 per split.
+// Split the input features over the CTAs of a cluster (at most 8) only while
+// the output tiles leave resident CTA slots empty, keeping at least 4 steps of
+// 64 input features per split.
 int linear_splits(const pkv_pool* pool, int tokens, int in, int out)
 {
     const int bn = linear_tile_tokens(tokens);
     const int tiles = (out / kBM) * ((tokens + bn - 1) / bn);
+    const int slots = pool->num_sms * (bn == 64 ? 2 : 1);
     int splits = 1;
-    while (tiles * splits * 2 <= pool->num_sms && (in / kBK) / (splits * 2) >= 4) splits *= 2;
+    while (splits < kMaxSplits && tiles * splits * 2 <= slots && (in / kBK) / (splits * 2) >= 4) splits *= 2;
     return splits;
 }
 
 cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in, int out,
-                          void* part, cudaStream_t s)
+                          cudaStream_t s)
 {
     LinParams p;
     p.y = static_cast<__nv_bfloat16*>(y);
-    p.part = static_cast<float*>(part);
     p.err = pool->err;
     p.tokens = tokens;
     p.in = in;
