@@ -425,12 +425,14 @@ def run_gpu(args) -> None:
 # ---------------------------------------------------------------------------- the projections (pkv_linear)
 
 LINEAR_SHAPES = (("q_proj", 4096, 4096), ("k_proj", 1024, 4096), ("v_proj", 1024, 4096), ("o_proj", 4096, 4096))
+# one step: q/k/v fused in one launch (pkv_qkv_proj), then o_proj (pkv_linear)
 
 
 def run_gpu_linear(args) -> None:
     """The four projections around one attention layer (q/k/v before it, o_proj
     after it) for `tokens` tokens: 64 (the decode batch) or 2048 (the prompts of
-    the step workload).  One step = four pkv_linear calls."""
+    the step workload).  One step = pkv_qkv_proj (q, k, v in one launch) and
+    pkv_linear (o_proj)."""
     import torch
     import paged_kv_gqa_qk_gb300 as pkv
     import workloads as W
@@ -448,13 +450,15 @@ def run_gpu_linear(args) -> None:
     host_x, _ = W.make_linear(tokens, 4096, 128, seed=rank_seed(3000 + tokens, rank))
     host_a, _ = W.make_linear(tokens, 4096, 128, seed=rank_seed(3001 + tokens, rank))  # the attention output
     ws = [W.make_linear(1, i, o, seed=rank_seed(3100 + j, rank))[1].to(dev) for j, (_, o, i) in enumerate(LINEAR_SHAPES)]
+    w_qkv = torch.cat(ws[:3], 0).contiguous()
     x, a = host_x.to(dev), host_a.to(dev)
     ys = [torch.empty(tokens, o, dtype=torch.bfloat16, device=dev) for _, o, _ in LINEAR_SHAPES]
+    q, k, v = (ys[0].view(tokens, 32, 128), ys[1].view(tokens, 8, 128), ys[2].view(tokens, 8, 128))
     stream = torch.cuda.Stream(device=dev)
 
     def step():
-        for j in range(4):
-            pool.linear(a if j == 3 else x, ws[j], ys[j], stream=stream)
+        pool.qkv_proj(x, w_qkv, q, k, v, stream=stream)
+        pool.linear(a, ws[3], ys[3], stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -511,8 +515,8 @@ def run_gpu_linear(args) -> None:
     weight_bytes = sum(2 * o * i for _, o, i in LINEAR_SHAPES)
     act_bytes = sum(2 * tokens * (i + o) for _, o, i in LINEAR_SHAPES)
     flops = sum(2 * tokens * o * i for _, o, i in LINEAR_SHAPES)
-    kern_s = k_ms / 1e3 / max(k_n, 1) * 4  # the four launches of one step
-    timing = "CUDA events around each matrix-product launch (four per step), second timed pass"
+    kern_s = k_ms / 1e3 / max(k_n, 1) * 2  # the two launches of one step
+    timing = "CUDA events around each matrix-product launch (two per step), second timed pass"
     if tokens <= 256:   # weight streaming: bound by HBM
         peak, peak_kind = measured_peak_hbm()
         roofline = {"bound": "hbm", "kernel": "linear_kernel", "achieved": (weight_bytes + act_bytes) / kern_s / 1e9,
@@ -546,8 +550,7 @@ def run_gpu_linear(args) -> None:
         "roofline": roofline,
         "e2e": {"value": tokens * args.steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": sum(1 + (pkv.pkv_linear_workspace_bytes(pool.handle, tokens, i, o) > 0)
-                            for _, o, i in LINEAR_SHAPES) * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
     pool.close()

@@ -274,6 +274,18 @@ PKV_API int pkv_linear_workspace_bytes(const pkv_pool* pool, int tokens, int in_
 PKV_API int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in_features,
                        int out_features, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The three projections before the attention in one launch: w_qkv is q_proj,
+ * k_proj and v_proj stacked row-wise, [(heads + 2 kv_heads) * head_dim][hidden]
+ * (the pool's config), and
+ *   q[t] = x[t] Wq^T  [tokens][heads][head_dim]
+ *   k[t] = x[t] Wk^T  [tokens][kv_heads][head_dim]
+ *   v[t] = x[t] Wv^T  [tokens][kv_heads][head_dim]
+ * the layouts pkv_decode / pkv_step / pkv_prefill take.  Same arithmetic as
+ * pkv_linear; hidden % 64 == 0 (PKV_ENOTIMPL otherwise); all pointers 16-byte
+ * aligned device memory. */
+PKV_API int pkv_qkv_proj(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden, void* q, void* k,
+                         void* v, void* stream);
+
 /* ---- decode without a caller workspace -------------------------------------------------------
  * The pages have no counterpart to this entry point; it is a convenience of
  * this library.  It is pkv_decode for callers that cannot allocate device

@@ -27,7 +27,7 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
                "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_prefill", "pkv_check_errors",
                "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static",
-               "pkv_linear_workspace_bytes", "pkv_linear")
+               "pkv_linear_workspace_bytes", "pkv_linear", "pkv_qkv_proj")
 
 # Size of the scratch array pkv_decode_static uses in place of a workspace.
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_decode_static": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp], i32),
         "pkv_linear_workspace_bytes": ([vp, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "pkv_linear": ([vp, vp, vp, vp, i32, i32, i32, vp, sz, vp], i32),
+        "pkv_qkv_proj": ([vp, vp, vp, i32, i32, vp, vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -252,6 +253,20 @@ def pkv_linear(pool, x, w, y, workspace=None, stream=None) -> None:
         _stream(stream)), "pkv_linear")
 
 
+def pkv_qkv_proj(pool, x, w_qkv, q, k, v, stream=None) -> None:
+    """q, k, v = x Wq^T, x Wk^T, x Wv^T with w_qkv = [Wq; Wk; Wv] stacked row-wise (one launch)."""
+    tokens, hidden = int(x.shape[0]), int(x.shape[1])
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.shape[0] != tokens:
+            raise ValueError(f"{name} has {t.shape[0]} tokens, x has {tokens}")
+    if w_qkv.dim() != 2 or w_qkv.shape[1] != hidden or w_qkv.shape[0] != q[0].numel() + k[0].numel() + v[0].numel():
+        raise ValueError(f"w_qkv {tuple(w_qkv.shape)} does not stack the q, k, v projections of x {tuple(x.shape)}")
+    _check(load_library().pkv_qkv_proj(
+        pool, _dev(x, torch.bfloat16, "x"), _dev(w_qkv, torch.bfloat16, "w_qkv"), tokens, hidden,
+        _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), _stream(stream)),
+        "pkv_qkv_proj")
+
+
 def pkv_check_errors(pool, stream=None) -> int:
     f = ctypes.c_uint32()
     _check(load_library().pkv_check_errors(pool, _stream(stream), ctypes.byref(f)), "pkv_check_errors")
@@ -335,6 +350,18 @@ class PagedKVPool:
             ws = self._lws
         pkv_linear(self.handle, x, w, y, ws, stream)
         return y
+
+    def qkv_proj(self, x, w_qkv, q=None, k=None, v=None, stream=None):
+        """q [tokens][heads][head_dim], k and v [tokens][kv_heads][head_dim] from x and the stacked weights."""
+        c, n = self.cfg, x.shape[0]
+        if q is None:
+            q = torch.empty(n, c.heads, c.head_dim, dtype=torch.bfloat16, device=x.device)
+        if k is None:
+            k = torch.empty(n, c.kv_heads, c.head_dim, dtype=torch.bfloat16, device=x.device)
+        if v is None:
+            v = torch.empty(n, c.kv_heads, c.head_dim, dtype=torch.bfloat16, device=x.device)
+        pkv_qkv_proj(self.handle, x, w_qkv, q, k, v, stream)
+        return q, k, v
 
     def check_errors(self, stream=None) -> int:
         return pkv_check_errors(self.handle, stream)

@@ -490,7 +490,29 @@ int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens
     if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_EWORKSPACE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
-    return launch_linear(pool, x, w, y, tokens, in_features, out_features, static_cast<cudaStream_t>(stream)) ==
+    void* ys[1] = {y};
+    const int widths[1] = {out_features};
+    return launch_linear(pool, x, w, tokens, in_features, 1, ys, widths, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_ECUDA;
+}
+
+int pkv_qkv_proj(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden, void* q, void* k, void* v,
+                 void* stream)
+{
+    if (!pool || !x || !w_qkv || !q || !k || !v) return PKV_EINVAL;
+    if (tokens <= 0 || hidden <= 0) return PKV_EINVAL;
+    if (hidden % 64) return PKV_ENOTIMPL;
+    if (tokens > (1 << 24) || hidden > (1 << 20)) return PKV_ERANGE;
+    if (!aligned(x, 16) || !aligned(w_qkv, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
+        return PKV_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    const int qw = pool->cfg.heads * pool->cfg.head_dim, kw = pool->cfg.kv_heads * pool->cfg.head_dim;
+    void* ys[3] = {q, k, v};
+    const int widths[3] = {qw, kw, kw};
+    return launch_linear(pool, x, w_qkv, tokens, hidden, 3, ys, widths, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? PKV_OK
                : PKV_ECUDA;

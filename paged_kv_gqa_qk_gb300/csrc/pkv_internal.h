@@ -94,8 +94,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
 // cluster), and the launch.
 int linear_tile_tokens(int tokens);
 int linear_splits(const pkv_pool* pool, int tokens, int in, int out);
-cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in, int out,
-                          cudaStream_t s);
+cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, int tokens, int in, int nseg,
+                          void* const* y, const int* widths, cudaStream_t s);
 
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.

@@ -47,11 +47,25 @@ struct LinShape {
     static constexpr int kAlloc = kTmemSlot + 16 + 1024;
 };
 
+// The output features split into up to three consecutive segments, each
+// written to its own [tokens][width] tensor (q, k, v of one fused projection);
+// segment boundaries are multiples of 128, so a tile lies in one segment.
 struct LinParams {
-    __nv_bfloat16* y;   // [tokens][out]
+    __nv_bfloat16* y[3];
+    int seg_end[3];     // cumulative widths; seg_end[2] == out
     uint32_t* err;
     int tokens, in, out, splits;
 };
+
+// The segment holding output tile row m0: its tensor, its width and the tile's column in it.
+__device__ __forceinline__ __nv_bfloat16* seg_of(const LinParams& p, int m0, int& width, int& col)
+{
+    const int s = m0 < p.seg_end[0] ? 0 : (m0 < p.seg_end[1] ? 1 : 2);
+    const int start = s ? p.seg_end[s - 1] : 0;
+    width = p.seg_end[s] - start;
+    col = m0 - start;
+    return p.y[s];
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
@@ -136,7 +150,9 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
     pdl_wait();  // y may be read by the kernel before this one
     const bool ok = mbar_wait(bar_done, 0);
     tc_fence_after();
-    const int o = m0 + 32 * warp + lane;
+    int yw, yc;
+    __nv_bfloat16* const y = seg_of(p, m0, yw, yc);
+    const int o = yc + 32 * warp + lane;  // this thread's column of y
     if (p.splits == 1) {
         if (ok) {
 #pragma unroll 1
@@ -147,7 +163,7 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = n0 + c0 + j;
-                    if (t < p.tokens) p.y[(int64_t)t * p.out + o] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    if (t < p.tokens) y[(int64_t)t * yw + o] = __float2bfloat16_rn(__uint_as_float(v[j]));
                 }
             }
         }
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
             uint2 o2;
             o2.x = pack_bf16(__float2bfloat16_rn(acc.x), __float2bfloat16_rn(acc.y));
             o2.y = pack_bf16(__float2bfloat16_rn(acc.z), __float2bfloat16_rn(acc.w));
-            *reinterpret_cast<uint2*>(p.y + (int64_t)(n0 + t) * p.out + m0 + f) = o2;
+            *reinterpret_cast<uint2*>(y + (int64_t)(n0 + t) * yw + yc + f) = o2;
         }
     }
     cluster_sync();  // no CTA leaves while another reads its shared memory
@@ -257,16 +273,21 @@ int linear_splits(const pkv_pool* pool, int tokens, int in, int out)
     return splits;
 }
 
-cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, void* y, int tokens, int in, int out,
-                          cudaStream_t s)
+cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, int tokens, int in, int nseg,
+                          void* const* y, const int* widths, cudaStream_t s)
 {
     LinParams p;
-    p.y = static_cast<__nv_bfloat16*>(y);
+    int end = 0;
+    for (int i = 0; i < 3; ++i) {
+        end += i < nseg ? widths[i] : 0;
+        p.y[i] = static_cast<__nv_bfloat16*>(i < nseg ? y[i] : nullptr);
+        p.seg_end[i] = end;
+    }
     p.err = pool->err;
     p.tokens = tokens;
     p.in = in;
-    p.out = out;
-    p.splits = linear_splits(pool, tokens, in, out);
+    p.out = end;
+    p.splits = linear_splits(pool, tokens, in, end);
     switch (linear_tile_tokens(tokens)) {
     case 64:
         return launch_linear_bn<64>(pool, x, w, p, p.splits, s);

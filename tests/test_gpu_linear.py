@@ -89,3 +89,20 @@ def test_linear_host_errors(pool):
     torch.cuda.synchronize()
     assert not y.any()
     assert pkv.pkv_linear_workspace_bytes(pool.handle, 8, 4096, 1024) == 0
+
+
+@pytest.mark.parametrize("tokens", [1, 64, 300])
+def test_qkv_proj_matches_oracle(pool, tokens):
+    """The fused projection writes q, k, v (each split into heads) as three separate linears would."""
+    c = pool.cfg
+    wq_rows, wk_rows = c.heads * c.head_dim, c.kv_heads * c.head_dim
+    x, w = W.make_linear(tokens, 512, wq_rows + 2 * wk_rows, seed=40 + tokens)
+    q, k, v = pool.qkv_proj(x.cuda(), w.cuda())
+    assert pool.check_errors() == 0
+    assert q.shape == (tokens, c.heads, c.head_dim) and k.shape == v.shape == (tokens, c.kv_heads, c.head_dim)
+    check(x, w[:wq_rows], q.reshape(tokens, -1).cpu(), f"qkv q {tokens}")
+    check(x, w[wq_rows:wq_rows + wk_rows], k.reshape(tokens, -1).cpu(), f"qkv k {tokens}")
+    check(x, w[wq_rows + wk_rows:], v.reshape(tokens, -1).cpu(), f"qkv v {tokens}")
+    # the same bits as the unfused product
+    y = pool.linear(x.cuda(), w.cuda())
+    assert torch.equal(torch.cat([q.reshape(tokens, -1), k.reshape(tokens, -1), v.reshape(tokens, -1)], 1), y)
