@@ -102,6 +102,10 @@ typedef struct {
     int max_seq;       /* positions must be < max_seq (length of the RoPE table) */
     double rope_theta; /* RoPE base */
     double eps;        /* QK-norm epsilon */
+    int rotary_dim;    /* RoPE rotates the first rotary_dim dims of each head (0 = all, the Qwen3 case);
+                          the partial form of the gated-attention variant (fantasma model.zig, applyRope:
+                          pairs (i, i + rotary_dim/2), inv_freq = theta^(-2i/rotary_dim)); built for
+                          multiples of 32, PKV_ENOTIMPL otherwise */
 } pkv_config;
 
 /* Fill *cfg with the Qwen3-8B defaults.  Returns PKV_OK or PKV_EINVAL (null). */
@@ -285,6 +289,18 @@ PKV_API int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, in
  * aligned device memory. */
 PKV_API int pkv_qkv_proj(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden, void* q, void* k,
                          void* v, void* stream);
+
+/* ---- output gate of the gated-attention variant ----------------------------------------
+ * fantasma model.zig, fullAttentionForward ("Full Attention (GQA with output gate +
+ * QK-norm + partial RoPE)"): the q projection also yields a gate per head and
+ * dim, and the attention output is multiplied by its sigmoid before o_proj:
+ *   out[t][h][d] *= 1 / (1 + exp(-gate[t][h][d]))     (fp32, rounded to bf16)
+ * With a pool whose rotary_dim is below head_dim (the variant's partial RoPE),
+ * pkv_decode / pkv_step / pkv_prefill followed by this call give that layer's
+ * attention.  Qwen3-8B has no gate.
+ *   out   device bf16 [tokens][heads][head_dim], updated in place, 16-byte aligned
+ *   gate  device bf16 [tokens][heads][head_dim], 16-byte aligned */
+PKV_API int pkv_output_gate(pkv_pool* pool, void* out, const void* gate, int tokens, void* stream);
 
 /* ---- decode without a caller workspace -------------------------------------------------------
  * The pages have no counterpart to this entry point; it is a convenience of

@@ -31,7 +31,7 @@ _lib = None
 # KvHeads 8, HeadDim 128, MaxSeq 40960), attention.linnet (PageSize 64),
 # rope.linnet (THETA 1e6), norm.linnet (eps 1e-6).
 DEFAULT_CONFIG = dict(heads=32, kv_heads=8, head_dim=128, page_size=64, max_seq=40960,
-                      rope_theta=1.0e6, eps=1.0e-6)
+                      rope_theta=1.0e6, eps=1.0e-6, rotary_dim=128)
 
 ERR_POSITION, ERR_PAGE, ERR_ROW, ERR_SLOT = 1, 2, 4, 8
 
@@ -39,7 +39,7 @@ ERR_POSITION, ERR_PAGE, ERR_ROW, ERR_SLOT = 1, 2, 4, 8
 class OrcConfig(ctypes.Structure):
     _fields_ = [("heads", ctypes.c_int), ("kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("max_seq", ctypes.c_int),
-                ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double), ("rotary_dim", ctypes.c_int)]
 
 
 def build(force: bool = False) -> str:
@@ -96,8 +96,12 @@ def _cfg(cfg: dict | None) -> OrcConfig:
     d = dict(DEFAULT_CONFIG)
     if cfg:
         d.update(cfg)
+    if cfg and "head_dim" in cfg and "rotary_dim" not in cfg:
+        d["rotary_dim"] = d["head_dim"]   # a custom head size rotates all of it unless told otherwise
+    if not 0 <= d["rotary_dim"] <= d["head_dim"] or d["rotary_dim"] % 2:
+        raise ValueError(f"rotary_dim {d['rotary_dim']} for head_dim {d['head_dim']}")
     return OrcConfig(d["heads"], d["kv_heads"], d["head_dim"], d["page_size"], d["max_seq"],
-                     float(d["rope_theta"]), float(d["eps"]))
+                     float(d["rope_theta"]), float(d["eps"]), int(d["rotary_dim"]))
 
 
 def _ptr(a: np.ndarray | None, ctype):
@@ -255,3 +259,11 @@ def linear(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
     src/attention.linnet: q_proj / k_proj / v_proj / o_proj), in float64 on the exact
     values of bf16 x [tokens][in] and w [out][in]; a library matrix product is the step."""
     return bf16_to_f64(_u16(x_bits)) @ bf16_to_f64(_u16(w_bits)).T
+
+
+def output_gate(out: np.ndarray, gate_bits: np.ndarray) -> np.ndarray:
+    """The output gate of the gated attention variant (fantasma model.zig,
+    fullAttentionForward: attn_out *= sigmoid(gate)), elementwise in float64 on
+    the attention output and the exact values of the bf16 gate."""
+    g = bf16_to_f64(_u16(gate_bits))
+    return np.asarray(out, dtype=np.float64) / (1.0 + np.exp(-g))

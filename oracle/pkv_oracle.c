@@ -43,6 +43,7 @@ typedef struct {
     int max_seq;      /* MaxSeq: bound on positions */
     double rope_theta;
     double eps;
+    int rotary_dim;   /* dims rotated by RoPE (the first rotary_dim); 0 = head_dim */
 } orc_config;
 
 /* Error bits reported for tokens the oracle skips (zero output, no write).
@@ -122,15 +123,18 @@ void orc_qk_norm(const orc_config* c, const uint16_t* x, const uint16_t* w, doub
  * [NEST] src/rope.linnet tables: inv_freq[i] = theta^(-2i/D) for i < D/2,
  * angle = pos * inv_freq[i], tables are concat(angles, angles).  [ZIG]
  * applyRope: the rotate-half form, x*cos + rotate_half(x)*sin with
- * rotate_half(x) = concat(-x2, x1).  So for i < D/2:
- *   y[i]       = x[i]       cos(a_i) - x[i+D/2] sin(a_i)
- *   y[i+D/2]   = x[i+D/2]   cos(a_i) + x[i]     sin(a_i)
- * Angles are formed in double (the pages use f32; see the readings). */
+ * rotate_half(x) = concat(-x2, x1), over the first rotary_dim = R dims only
+ * (Qwen3: R = D; the hybrid model of the Zig page rotates part of each head,
+ * its tables built with inv_freq[i] = theta^(-2i/R)).  So for i < R/2:
+ *   y[i]       = x[i]       cos(a_i) - x[i+R/2] sin(a_i)
+ *   y[i+R/2]   = x[i+R/2]   cos(a_i) + x[i]     sin(a_i)
+ * and y[d] = x[d] for d >= R.  Angles are formed in double (the pages use
+ * f32; see the readings). */
 void orc_rope(const orc_config* c, double* y, int pos)
 {
-    const int D = c->head_dim, half = D / 2;
+    const int R = (c->rotary_dim > 0 && c->rotary_dim < c->head_dim) ? c->rotary_dim : c->head_dim, half = R / 2;
     for (int i = 0; i < half; ++i) {
-        double inv_freq = pow(c->rope_theta, -2.0 * (double)i / (double)D);
+        double inv_freq = pow(c->rope_theta, -2.0 * (double)i / (double)R);
         double a = (double)pos * inv_freq;
         double cs = cos(a), sn = sin(a);
         double x1 = y[i], x2 = y[i + half];

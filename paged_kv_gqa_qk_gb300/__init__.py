@@ -27,7 +27,7 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
                "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_prefill", "pkv_check_errors",
                "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static",
-               "pkv_linear_workspace_bytes", "pkv_linear", "pkv_qkv_proj")
+               "pkv_linear_workspace_bytes", "pkv_linear", "pkv_qkv_proj", "pkv_output_gate")
 
 # Size of the scratch array pkv_decode_static uses in place of a workspace.
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
@@ -36,7 +36,7 @@ PKV_STATIC_SCRATCH_BYTES = 32 << 20
 class PkvConfig(ctypes.Structure):
     _fields_ = [("heads", ctypes.c_int), ("kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("max_seq", ctypes.c_int),
-                ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double), ("rotary_dim", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_linear_workspace_bytes": ([vp, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "pkv_linear": ([vp, vp, vp, vp, i32, i32, i32, vp, sz, vp], i32),
         "pkv_qkv_proj": ([vp, vp, vp, i32, i32, vp, vp, vp, vp], i32),
+        "pkv_output_gate": ([vp, vp, vp, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -265,6 +266,14 @@ def pkv_qkv_proj(pool, x, w_qkv, q, k, v, stream=None) -> None:
         pool, _dev(x, torch.bfloat16, "x"), _dev(w_qkv, torch.bfloat16, "w_qkv"), tokens, hidden,
         _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), _stream(stream)),
         "pkv_qkv_proj")
+
+
+def pkv_output_gate(pool, out, gate, stream=None) -> None:
+    """out *= sigmoid(gate) in place (the gated-attention variant's output gate)."""
+    if out.shape != gate.shape:
+        raise ValueError(f"gate {tuple(gate.shape)} does not match out {tuple(out.shape)}")
+    _check(load_library().pkv_output_gate(pool, _dev(out, torch.bfloat16, "out"), _dev(gate, torch.bfloat16, "gate"),
+                                          int(out.shape[0]), _stream(stream)), "pkv_output_gate")
 
 
 def pkv_check_errors(pool, stream=None) -> int:

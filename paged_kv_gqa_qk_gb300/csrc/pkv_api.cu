@@ -156,6 +156,8 @@ static int check_config(const pkv_config* c)
     if (c->head_dim != kHeadDim || c->page_size != kPageSize || c->heads != kGroup * c->kv_heads)
         return PKV_ENOTIMPL;
     if (c->max_seq > (1 << 20) || c->kv_heads > 256) return PKV_ERANGE;
+    if (c->rotary_dim < 0 || c->rotary_dim > c->head_dim || c->rotary_dim % 2) return PKV_EINVAL;
+    if (c->rotary_dim % 32) return PKV_ENOTIMPL;
     return PKV_OK;
 }
 
@@ -165,15 +167,18 @@ static int check_config(const pkv_config* c)
 // position 40959 is off by up to ~2e-3 rad) and kept as two fp32 tables: hi,
 // the nearest fp32 values (q uses these), and lo, the remainders (k uses
 // hi + lo, so its rotation keeps the double table's accuracy).
+// (cos, sin) of pos * theta^(-2i/R) for i < R/2 (R = rotary dims), in double,
+// kept as the nearest fp32 pair plus the fp32 of the remainder; entries past
+// R/2 (partial rotation) are the identity (1, 0).
 static void rope_tables(const pkv_config& c, std::vector<float2>& hi, std::vector<float2>& lo)
 {
-    const int half = c.head_dim / 2;
-    hi.resize((size_t)c.max_seq * half);
-    lo.resize((size_t)c.max_seq * half);
-    std::vector<double> inv(half);
-    for (int i = 0; i < half; ++i) inv[i] = std::pow(c.rope_theta, -2.0 * i / (double)c.head_dim);
+    const int half = c.head_dim / 2, R = c.rotary_dim > 0 ? c.rotary_dim : c.head_dim, rhalf = R / 2;
+    hi.assign((size_t)c.max_seq * half, make_float2(1.f, 0.f));
+    lo.assign((size_t)c.max_seq * half, make_float2(0.f, 0.f));
+    std::vector<double> inv(rhalf);
+    for (int i = 0; i < rhalf; ++i) inv[i] = std::pow(c.rope_theta, -2.0 * i / (double)R);
     for (int p = 0; p < c.max_seq; ++p)
-        for (int i = 0; i < half; ++i) {
+        for (int i = 0; i < rhalf; ++i) {
             const double a = (double)p * inv[i];
             const double cs = std::cos(a), sn = std::sin(a);
             const float ch = (float)cs, sh = (float)sn;
@@ -342,6 +347,7 @@ int pkv_config_default(pkv_config* cfg)
     cfg->max_seq = 40960;
     cfg->rope_theta = 1.0e6;
     cfg->eps = 1.0e-6;
+    cfg->rotary_dim = 128;
     return PKV_OK;
 }
 
@@ -516,6 +522,17 @@ int pkv_qkv_proj(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, i
                    cudaSuccess
                ? PKV_OK
                : PKV_ECUDA;
+}
+
+int pkv_output_gate(pkv_pool* pool, void* out, const void* gate, int tokens, void* stream)
+{
+    if (!pool || !out || !gate || tokens <= 0) return PKV_EINVAL;
+    if (tokens > (1 << 24)) return PKV_ERANGE;
+    if (!aligned(out, 16) || !aligned(gate, 16)) return PKV_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    const int64_t n = (int64_t)tokens * pool->cfg.heads * pool->cfg.head_dim;
+    return launch_gate(pool, out, gate, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags)

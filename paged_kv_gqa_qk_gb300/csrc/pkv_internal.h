@@ -97,6 +97,9 @@ int linear_splits(const pkv_pool* pool, int tokens, int in, int out);
 cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, int tokens, int in, int nseg,
                           void* const* y, const int* widths, cudaStream_t s);
 
+// out *= sigmoid(gate) over n bf16 elements (n % 8 == 0, 16-byte aligned).
+cudaError_t launch_gate(const pkv_pool* pool, void* out, const void* gate, int64_t n, cudaStream_t s);
+
 // Per-device kernel attributes (dynamic shared memory); called with the
 // pool's device current when a pool is created.
 cudaError_t configure_kernels();

@@ -69,12 +69,34 @@ __device__ __forceinline__ float rotate_exact(float u, float up, float2 hi, floa
     return __fadd_rn(s, lo_terms);
 }
 
+// RoPE layout of a warp holding one head, 4 consecutive dims per lane: with R
+// rotated dims, lanes below R/8 hold the first rotary half (partner: R/2
+// dims, i.e. R/8 lanes, up), lanes in [R/8, R/4) the second (partner R/8 lanes
+// down), and lanes from R/4 up the dims RoPE leaves as they are.
+struct KRope {
+    int src;     // lane holding this lane's partner dims
+    float sgn;   // -1: first half (u cos - partner sin), +1: second (u cos + partner sin)
+    int f0;      // table index of this lane's first dim
+    bool rot;    // false: not rotated
+};
+__device__ __forceinline__ KRope krope(int lane, int rot)
+{
+    const int hl = rot / 8;
+    KRope r;
+    r.rot = lane < 2 * hl;
+    const bool first = lane < hl;
+    r.src = first ? lane + hl : (r.rot ? lane - hl : lane);
+    r.sgn = first ? -1.f : 1.f;
+    r.f0 = r.rot ? 4 * (first ? lane : lane - hl) : 0;
+    return r;
+}
+
 // The warp's normed + roped k as 4 bf16 (this lane's elements).
 //   kraw: this lane's 4 raw bf16;  wk: its k_norm weights;
-//   rh/rl: (cos, sin) hi and lo parts of this lane's 4 rotation frequencies
-//   4 (lane % 16) .. 4 (lane % 16) + 3 at the token's position.
+//   rh/rl: (cos, sin) hi and lo parts at the token's position for this lane's
+//   table entries krope(lane, rot).f0 .. + 3;  rot: the rotated dims.
 __device__ __forceinline__ uint2 norm_rope_k_regs(uint2 kraw, const float (&wk)[4], const float2 (&rh)[4],
-                                                  const float2 (&rl)[4], float eps, int lane)
+                                                  const float2 (&rl)[4], float eps, int lane, int rot)
 {
     float x[4];
     unpack4(kraw, x);
@@ -82,37 +104,29 @@ __device__ __forceinline__ uint2 norm_rope_k_regs(uint2 kraw, const float (&wk)[
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
     const float inv = rsqrtf(ss * (1.0f / kHeadDim) + eps);
-    const float sgn = lane < 16 ? -1.f : 1.f;
+    const KRope kr = krope(lane, rot);
     __nv_bfloat16 r[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float u = x[i] * wk[i];
-        const float partner = sgn * __shfl_xor_sync(kFull, u, 16);
-        r[i] = __float2bfloat16_rn(__fmul_rn(rotate_exact(u, partner, rh[i], rl[i]), inv));
+        const float partner = kr.sgn * __shfl_sync(kFull, u, kr.src);
+        r[i] = __float2bfloat16_rn(__fmul_rn(kr.rot ? rotate_exact(u, partner, rh[i], rl[i]) : u, inv));
     }
     return make_uint2(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]));
 }
 
 //   rhi/rlo: (cos, sin) hi and lo parts of the token's position, [64].
 __device__ __forceinline__ uint2 norm_rope_k(uint2 kraw, const float (&wk)[4], const float2* rhi, const float2* rlo,
-                                             float eps, int lane)
+                                             float eps, int lane, int rot)
 {
-    float x[4];
-    unpack4(kraw, x);
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-    const float inv = rsqrtf(ss * (1.0f / kHeadDim) + eps);
-    const float sgn = lane < 16 ? -1.f : 1.f;
-    __nv_bfloat16 r[4];
+    const KRope kr = krope(lane, rot);
+    float2 rh[4], rl[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int f = 4 * (lane & 15) + i;
-        const float u = x[i] * wk[i];
-        const float partner = sgn * __shfl_xor_sync(kFull, u, 16);
-        r[i] = __float2bfloat16_rn(__fmul_rn(rotate_exact(u, partner, rhi[f], rlo[f]), inv));
+        rh[i] = rhi[kr.f0 + i];
+        rl[i] = rlo[kr.f0 + i];
     }
-    return make_uint2(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]));
+    return norm_rope_k_regs(kraw, wk, rh, rl, eps, lane, rot);
 }
 
 // =====================================================================================
@@ -127,7 +141,7 @@ struct PrepParams {
     const int32_t* slots;           // [P] or null
     const int32_t* step_positions;  // [rows]
     const int32_t* table;           // [rows][pages], or null: contiguous rows
-    int P, rows, pages, num_pages, max_seq, kv_heads;
+    int P, rows, pages, num_pages, max_seq, kv_heads, rot;
     int64_t num_slots;
     float eps;
     const float2* rope_hi;          // (cos, sin) [max_seq][64], fp32 nearest to the double values
@@ -195,8 +209,9 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
     }
     float2 rh[4], rl[4];
     {
-        const float4* h4 = reinterpret_cast<const float4*>(p.rope_hi + (int64_t)pc * kRopeHalf + 4 * (lane & 15));
-        const float4* l4 = reinterpret_cast<const float4*>(p.rope_lo + (int64_t)pc * kRopeHalf + 4 * (lane & 15));
+        const int f0 = krope(lane, p.rot).f0;
+        const float4* h4 = reinterpret_cast<const float4*>(p.rope_hi + (int64_t)pc * kRopeHalf + f0);
+        const float4* l4 = reinterpret_cast<const float4*>(p.rope_lo + (int64_t)pc * kRopeHalf + f0);
         const float4 a = h4[0], b = h4[1], c = l4[0], d = l4[1];
         rh[0] = make_float2(a.x, a.y), rh[1] = make_float2(a.z, a.w), rh[2] = make_float2(b.x, b.y),
         rh[3] = make_float2(b.z, b.w);
@@ -229,7 +244,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
             kr = *reinterpret_cast<const uint2*>(p.k + src);
             vr = *reinterpret_cast<const uint2*>(p.v + src);
         }
-        *reinterpret_cast<uint2*>(p.K + dst) = norm_rope_k_regs(kr, wk, rh, rl, p.eps, lane);
+        *reinterpret_cast<uint2*>(p.K + dst) = norm_rope_k_regs(kr, wk, rh, rl, p.eps, lane, p.rot);
         *reinterpret_cast<uint2*>(p.V + dst) = vr;  // v is written as given
     }
 }
@@ -251,6 +266,7 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.num_pages = pool->num_pages;
     p.max_seq = pool->cfg.max_seq;
     p.kv_heads = pool->cfg.kv_heads;
+    p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.num_slots = pool->num_slots;
     p.eps = static_cast<float>(pool->cfg.eps);
     p.rope_hi = pool->rope_hi;
@@ -295,6 +311,53 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
 // its staged copy of the page and to the pool.  Each (row, kv head) slot is
 // read only by that row (a documented condition of pkv_decode), so no other
 // CTA waits for the write.
+// B fragments of q for one head: the dims 16 ks + 2 tig + {0, 1, 8, 9} (ks < 8)
+// this lane holds, normed (xr raw, wq2 weights, inv = 1/rms times the score
+// scale) and rotated with the pairs (d, d + 16 HK) of a 32 HK-dim rotation
+// (rpf: the position's (cos, sin) table), dims from 32 HK up unrotated; split
+// into a bf16 head (prt 0) or the bf16 of its remainder (prt 1).
+template <int HK>
+__device__ __forceinline__ void q_prep(const uint32_t (&xr)[8][2], const uint32_t (&wq2)[8][2], const float2* rpf,
+                                       float inv, int tig, int prt, uint32_t (&bq)[8][2])
+{
+    auto part = [&](const float (&y)[4], uint32_t (&dst)[2]) {
+        __nv_bfloat16 h[4], t[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) split_bf16(y[k], h[k], t[k]);
+        dst[0] = prt ? pack_bf16(t[0], t[1]) : pack_bf16(h[0], h[1]);
+        dst[1] = prt ? pack_bf16(t[2], t[3]) : pack_bf16(h[2], h[3]);
+    };
+    auto u_of = [&](uint32_t x, uint32_t w, int b) {
+        return __uint_as_float(b ? (x & 0xffff0000u) : (x << 16)) * __uint_as_float(b ? (w & 0xffff0000u) : (w << 16));
+    };
+#pragma unroll
+    for (int ks = 0; ks < HK; ++ks) {  // dims d (ks) and their partners d + 16 HK (ks + HK)
+        float ylo[4], yhi[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int d = 16 * ks + 2 * tig + 8 * e + b;  // < 16 HK
+                const float ul = u_of(xr[ks][e], wq2[ks][e], b), uh = u_of(xr[ks + HK][e], wq2[ks + HK][e], b);
+                const float2 cs = rpf[d];
+                ylo[2 * e + b] = inv * (ul * cs.x - uh * cs.y);  // y[d]         = u[d] cos - u[d+16HK] sin
+                yhi[2 * e + b] = inv * (uh * cs.x + ul * cs.y);  // y[d + 16 HK] = u[d+16HK] cos + u[d] sin
+            }
+        }
+        part(ylo, bq[ks]);
+        part(yhi, bq[ks + HK]);
+    }
+#pragma unroll
+    for (int ks = 2 * HK; ks < 8; ++ks) {  // dims RoPE leaves as they are
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) y[2 * e + b] = inv * u_of(xr[ks][e], wq2[ks][e], b);
+        part(y, bq[ks]);
+    }
+}
+
 struct AttnParams {
     const __nv_bfloat16* q;   // [ntok][heads][128] projected q (normed + roped here)
     const __nv_bfloat16* k;   // [ntok][kv_heads][128]  (decode mode: appended here)
@@ -315,7 +378,7 @@ struct AttnParams {
     int32_t* prefix;          // [ntok + 1], written by CTA 0 for combine_kernel
     int32_t* unit_ok;         // [U], written by the CTA holding each unit's first page
     uint32_t* err;
-    int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode;
+    int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode, rot;
     int64_t num_slots;
     float eps;
 };
@@ -673,42 +736,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                 ss += __shfl_xor_sync(kFull, ss, 1);
                 ss += __shfl_xor_sync(kFull, ss, 2);
                 const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * qscale;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {  // dims d (ks) and their partners d + 64 (ks + 4)
-                    float ylo[4], yhi[4];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const int d = 16 * ks + 2 * tig + 8 * e + b;  // < 64
-                            const uint32_t xl = xr[ks][e], xh = xr[ks + 4][e];
-                            const uint32_t wl = wq2[ks][e], wh = wq2[ks + 4][e];
-                            const float ul = __uint_as_float(b ? (xl & 0xffff0000u) : (xl << 16)) *
-                                             __uint_as_float(b ? (wl & 0xffff0000u) : (wl << 16));
-                            const float uh = __uint_as_float(b ? (xh & 0xffff0000u) : (xh << 16)) *
-                                             __uint_as_float(b ? (wh & 0xffff0000u) : (wh << 16));
-                            const float2 cs = rpf[d];
-                            const float cf = cs.x, sf = cs.y;
-                            ylo[2 * e + b] = inv * (ul * cf - uh * sf);  // y[d]      = u[d] cos - u[d+64] sin
-                            yhi[2 * e + b] = inv * (uh * cf + ul * sf);  // y[d + 64] = u[d+64] cos + u[d] sin
-                        }
-                    }
-                    __nv_bfloat16 hl[4], tl[4], hh2[4], th[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        split_bf16(ylo[k], hl[k], tl[k]);
-                        split_bf16(yhi[k], hh2[k], th[k]);
-                    }
-                    bq[ks][0] = prt ? pack_bf16(tl[0], tl[1]) : pack_bf16(hl[0], hl[1]);
-                    bq[ks][1] = prt ? pack_bf16(tl[2], tl[3]) : pack_bf16(hl[2], hl[3]);
-                    bq[ks + 4][0] = prt ? pack_bf16(th[0], th[1]) : pack_bf16(hh2[0], hh2[1]);
-                    bq[ks + 4][1] = prt ? pack_bf16(th[2], th[3]) : pack_bf16(hh2[2], hh2[3]);
+                switch (p.rot) {  // rotated dims: pairs (d, d + rot / 2)
+                case 128: q_prep<4>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                case 96: q_prep<3>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                case 64: q_prep<2>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                default: q_prep<1>(xr, wq2, rpf, inv, tig, prt, bq); break;
                 }
             }
             // the warp that owns the new slot's position prepares the row's k and v
             if ((flags & kFlagHasLast) && warp == ((len - 1) % kPageSize) / 16) {
                 knew = norm_rope_k(*reinterpret_cast<const uint2*>(side + kSideK + 8 * lane), wk, rpf,
-                                   reinterpret_cast<const float2*>(side + kSideRopeLo), p.eps, lane);
+                                   reinterpret_cast<const float2*>(side + kSideRopeLo), p.eps, lane, p.rot);
                 vnew = *reinterpret_cast<const uint2*>(side + kSideV + 8 * lane);
             }
 #pragma unroll
@@ -953,6 +991,7 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.decode_mode = decode_mode ? 1 : 0;
+    p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.num_slots = pool->num_slots;
     p.eps = static_cast<float>(pool->cfg.eps);
 
@@ -1069,6 +1108,41 @@ cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+}
+
+// =====================================================================================
+// output gate of the gated-attention variant: out *= sigmoid(gate), elementwise
+// (fantasma model.zig, fullAttentionForward: "attn_out *= sigmoid(gate)")
+// =====================================================================================
+__global__ void __launch_bounds__(256) gate_kernel(__nv_bfloat16* out, const __nv_bfloat16* gate, int64_t n8)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 o = reinterpret_cast<const uint4*>(out)[i], g = reinterpret_cast<const uint4*>(gate)[i];
+        const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float y[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const float x = __uint_as_float(b ? (ov[e] & 0xffff0000u) : (ov[e] << 16));
+                const float z = __uint_as_float(b ? (gv[e] & 0xffff0000u) : (gv[e] << 16));
+                y[b] = x / (1.f + expf(-z));
+            }
+            const __nv_bfloat162 t = __floats2bfloat162_rn(y[0], y[1]);
+            r[e] = *reinterpret_cast<const uint32_t*>(&t);
+        }
+        reinterpret_cast<uint4*>(out)[i] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+}
+
+cudaError_t launch_gate(const pkv_pool* pool, void* out, const void* gate, int64_t n, cudaStream_t s)
+{
+    const int64_t n8 = n / 8;
+    const int64_t want = (n8 + 255) / 256, cap = 8LL * pool->num_sms;
+    gate_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(static_cast<__nv_bfloat16*>(out),
+                                                                    static_cast<const __nv_bfloat16*>(gate), n8);
+    return cudaGetLastError();
 }
 
 }  // namespace pkv

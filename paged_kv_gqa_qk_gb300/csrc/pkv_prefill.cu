@@ -104,7 +104,7 @@ struct PfParams {
     __nv_bfloat16* out;       // [P + rows][heads][128]
     int32_t* sched;           // unit counter, zero at launch
     uint32_t* err;
-    int P, pages, heads, kv_heads, ntiles;
+    int P, pages, heads, kv_heads, ntiles, rot;
     float eps;
 };
 
@@ -448,10 +448,20 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
                 }
                 const float inv =
                     rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * (1.4426950408889634f * 0.088388347648318440f);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // dims 8k..8k+7 of the first half and their partners 64 apart
-                    const uint4 rl = qchunk(k), rh = qchunk(k + 8);
-                    const uint4 wl = wsm[k], wh = wsm[k + 8];
+                // chunk c (dims 8c..8c+7) goes to Q half c / 8, chunk c % 8 of the row
+                auto store = [&](int c, const uint32_t (&w)[4]) {
+                    *reinterpret_cast<uint4*>(q0 + (c >> 3) * (kRowsM * 128) + sw128(m, 8 * (c & 7))) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                };
+                auto u_of = [](uint32_t x, uint32_t w, int b) {
+                    return __uint_as_float(b ? (x & 0xffff0000u) : (x << 16)) *
+                           __uint_as_float(b ? (w & 0xffff0000u) : (w << 16));
+                };
+                const int hc = p.rot / 16;  // chunks in a rotary half: chunk k pairs with k + hc
+#pragma unroll 4
+                for (int k = 0; k < hc; ++k) {  // dims 8k..8k+7 and their partners rot/2 further
+                    const uint4 rl = qchunk(k), rh = qchunk(k + hc);
+                    const uint4 wl = wsm[k], wh = wsm[k + hc];
                     const uint32_t xl[4] = {rl.x, rl.y, rl.z, rl.w}, xh[4] = {rh.x, rh.y, rh.z, rh.w};
                     const uint32_t vl[4] = {wl.x, wl.y, wl.z, wl.w}, vh[4] = {wh.x, wh.y, wh.z, wh.w};
                     uint32_t lo[4], hi[4];
@@ -462,22 +472,30 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
                             *reinterpret_cast<const float4*>(rs + 16 * ((4 * k + e) ^ sw));
 #pragma unroll
                         for (int b = 0; b < 2; ++b) {
-                            const float ul = __uint_as_float(b ? (xl[e] & 0xffff0000u) : (xl[e] << 16)) *
-                                             __uint_as_float(b ? (vl[e] & 0xffff0000u) : (vl[e] << 16));
-                            const float uh = __uint_as_float(b ? (xh[e] & 0xffff0000u) : (xh[e] << 16)) *
-                                             __uint_as_float(b ? (vh[e] & 0xffff0000u) : (vh[e] << 16));
+                            const float ul = u_of(xl[e], vl[e], b), uh = u_of(xh[e], vh[e], b);
                             const float co = b ? cc.z : cc.x, si = b ? cc.w : cc.y;
-                            y[b] = inv * (ul * co - uh * si);  // y[d]      = u[d] cos - u[d+64] sin
-                            z[b] = inv * (uh * co + ul * si);  // y[d + 64] = u[d+64] cos + u[d] sin
+                            y[b] = inv * (ul * co - uh * si);  // y[d]         = u[d] cos - u[d+rot/2] sin
+                            z[b] = inv * (uh * co + ul * si);  // y[d + rot/2] = u[d+rot/2] cos + u[d] sin
                         }
                         const __nv_bfloat162 yl = __floats2bfloat162_rn(y[0], y[1]);
                         const __nv_bfloat162 zh = __floats2bfloat162_rn(z[0], z[1]);
                         lo[e] = *reinterpret_cast<const uint32_t*>(&yl);
                         hi[e] = *reinterpret_cast<const uint32_t*>(&zh);
                     }
-                    *reinterpret_cast<uint4*>(q0 + sw128(m, 8 * k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4*>(q0 + kRowsM * 128 + sw128(m, 8 * k)) =
-                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    store(k, lo);
+                    store(k + hc, hi);
+                }
+                for (int c = 2 * hc; c < kHeadDim / 8; ++c) {  // dims RoPE leaves as they are
+                    const uint4 r = qchunk(c), w = wsm[c];
+                    const uint32_t x4[4] = {r.x, r.y, r.z, r.w}, w4[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 t = __floats2bfloat162_rn(inv * u_of(x4[e], w4[e], 0),
+                                                                       inv * u_of(x4[e], w4[e], 1));
+                        o4[e] = *reinterpret_cast<const uint32_t*>(&t);
+                    }
+                    store(c, o4);
                 }
             } else {
 #pragma unroll
@@ -809,6 +827,7 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.ntiles = (a.P + kTileTok - 1) / kTileTok;
+    p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.eps = static_cast<float>(pool->cfg.eps);
     const int units = p.ntiles * p.kv_heads;
     cudaLaunchConfig_t cfg = {};

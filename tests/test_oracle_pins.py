@@ -103,6 +103,37 @@ def test_rope_equals_complex_rotation():
         np.testing.assert_allclose(got[D // 2:], z.imag, rtol=0, atol=1e-11)
 
 
+@pytest.mark.parametrize("rot", [32, 64, 96])
+def test_partial_rope_rotates_only_the_first_dims(rot):
+    """rotary_dim R < head_dim (the gated variant's partial RoPE): dims from R on
+    are left exactly as they are; the first R are the complex rotation of the
+    pairs (i, i + R/2) by pos * theta^(-2i/R)."""
+    rng = np.random.default_rng(rot)
+    cfg = dict(CFG, rotary_dim=rot)
+    for pos in [0, 1, 77, 40959]:
+        y = rng.standard_normal(D)
+        out = oracle.rope(y, pos, cfg)
+        np.testing.assert_array_equal(out[rot:], y[rot:])
+        i = np.arange(rot // 2)
+        z = (y[:rot // 2] + 1j * y[rot // 2:rot]) * np.exp(1j * pos * np.power(1.0e6, -2.0 * i / rot))
+        # angles up to ~4e4 rad: one ulp of the frequency moves them by ~1e-11
+        np.testing.assert_allclose(out[:rot], np.concatenate([z.real, z.imag]), rtol=1e-10, atol=1e-10)
+    # rotary_dim = head_dim is the full rotation
+    y = rng.standard_normal(D)
+    np.testing.assert_array_equal(oracle.rope(y, 123, dict(CFG, rotary_dim=D)), oracle.rope(y, 123, CFG))
+
+
+def test_output_gate_closed_forms():
+    """out * sigmoid(gate): a zero gate halves, a large gate keeps, a very negative gate zeroes."""
+    out = np.array([[1.0, -3.0, 2.5, 0.0]])
+    gate = W.bits(torch.tensor([[0.0, 30.0, -30.0, 5.0]], dtype=torch.bfloat16))
+    got = oracle.output_gate(out, gate)
+    assert got[0, 0] == 0.5
+    assert abs(got[0, 1] + 3.0) < 1e-12 and abs(got[0, 2]) < 1e-12 and got[0, 3] == 0.0
+    g = float(oracle.bf16_to_f64(gate)[0, 1])
+    assert got[0, 1] == -3.0 / (1.0 + math.exp(-g))
+
+
 def test_rope_closed_form_and_invariants():
     rng = np.random.default_rng(5)
     y = rng.standard_normal(D)

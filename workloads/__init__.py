@@ -28,7 +28,7 @@ from dataclasses import dataclass, field
 import torch
 
 DEFAULT_CONFIG = dict(heads=32, kv_heads=8, head_dim=128, page_size=64, max_seq=40960,
-                      rope_theta=1.0e6, eps=1.0e-6)
+                      rope_theta=1.0e6, eps=1.0e-6, rotary_dim=128)
 
 # Bytes of K and V one position occupies across all kv heads (bf16).
 def kv_bytes_per_position(cfg: dict) -> int:
