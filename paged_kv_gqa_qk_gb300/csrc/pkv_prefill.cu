@@ -60,7 +60,7 @@ constexpr int kProducer = 4 * kGroups, kIssuer = kProducer + 1;
 constexpr int kPfThreads = 32 * 4 * (kGroups + 1);  // three warpgroups; warps 10 and 11 only take part in barriers
 // Registers per thread: the launch gives every thread kRegsLaunch; the third
 // warpgroup (producer, issuer) hands registers to the two softmax groups.
-constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 224, kRegsOther = 56;
+constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 200, kRegsOther = 104;
 static_assert(kGroups * 128 * kRegsSoftmax + 128 * kRegsOther <= kPfThreads * kRegsLaunch, "register split");
 static_assert(kRegsLaunch * kPfThreads <= 65536, "register file");
 constexpr uint32_t kTmemCols = 512;            // group h: S/P at 256h, O at 256h + 128
@@ -196,8 +196,12 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t vs, int h, int 
     const uint32_t d = tmem + 256 * h + 128, a = tmem + 256 * h;
     umma_bf16_ts(d, a, b0, id_pv, accumulate);
 #pragma unroll
-    for (int k = 1; k < kBlockKeys / 16; ++k)
-        if (k < npg * (kPageSize / 16)) umma_bf16_ts_acc(d, a + 8 * k, b0 + ((k * 2048) >> 4), id_pv);
+    for (int k = 1; k < kPageSize / 16; ++k) umma_bf16_ts_acc(d, a + 8 * k, b0 + ((k * 2048) >> 4), id_pv);
+    if (npg == 2) {  // the block's second page: one branch, not one per product
+#pragma unroll
+        for (int k = kPageSize / 16; k < kBlockKeys / 16; ++k)
+            umma_bf16_ts_acc(d, a + 8 * k, b0 + ((k * 2048) >> 4), id_pv);
+    }
 }
 
 // Every role runs its own unit loop through the same four CTA barriers per
