@@ -24,7 +24,9 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of one call: per token its attended length and table row (step
 // mode), the prefix of pages over tokens, a validity flag per (token, kv head)
 // unit, and one partial (4 heads x 128 fp32 + 4 log-sum-exps) per piece of a
-// unit split between CTAs: unit u's piece in CTA c sits at u + c, so U + C slots.
+// unit split between intervals of the attention's work split: unit u's piece in
+// interval i sits at u + i, and there are at most C static slices plus
+// kDynChunksPerCta * C chunks, so U + C (1 + kDynChunksPerCta) slots.
 Plan make_plan(const pkv_pool* pool, int tokens, int pages)
 {
     Plan pl;
@@ -33,7 +35,7 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
     pl.ctas = pool->ctas_override > 0 ? pool->ctas_override : pool->ctas_per_sm * pool->num_sms;
     const size_t G = (size_t)pool->cfg.kv_heads;
     const size_t units = (size_t)tokens * G;
-    const size_t slots = units + (size_t)pl.ctas;
+    const size_t slots = units + (size_t)pl.ctas * (1 + kDynChunksPerCta);
     size_t off = 0;
     pl.off_len = off;
     off = align_up(off + sizeof(int32_t) * tokens, 256);
@@ -50,6 +52,7 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
     pl.off_sched = off;
     off = align_up(off + sizeof(int32_t), 256);
     pl.total = off;
+    pl.claim = nullptr;
     return pl;
 }
 
@@ -77,6 +80,7 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
     }
     StepArgs as = a;  // the tokens the attention + combine kernels see
     Plan ps = plan;
+    ps.claim = pool->claims + (pool->call_seq++ % kClaimSlots);
     if (!decode) {
         if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
         if (launch_prefill(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
@@ -230,6 +234,8 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
         pkv_pool_free(p);
         return PKV_ENOMEM;
     }
+    p->claims = p->err + 32;
+    static_assert(32 + kClaimSlots <= 256 / 4, "the claim counters share the error word's allocation");
     std::vector<float2> rhi, rlo;
     rope_tables(*cfg, rhi, rlo);
     bool ok = true;

@@ -20,6 +20,12 @@ constexpr int kRopeHalf = kHeadDim / 2;
 
 constexpr int kTimerSlots = 4096;
 
+// The attention kernel's work split (see split_of in the kernels): after its
+// static slice a CTA claims chunks from a counter; at most kDynChunksPerCta
+// chunks per CTA, kept in one of kClaimSlots counters that calls take in turn.
+constexpr int kDynChunksPerCta = 16;
+constexpr int kClaimSlots = 32;
+
 }  // namespace pkv
 
 struct pkv_pool {
@@ -33,7 +39,9 @@ struct pkv_pool {
     void* v;
     float2* rope_hi;       // (cos, sin) [max_seq][head_dim/2]: fp32 nearest to the double values
     float2* rope_lo;       // the double values minus rope_hi, in fp32
-    uint32_t* err;         // sticky device error word
+    uint32_t* err;         // sticky device error word (word 0 of a 256-byte allocation)
+    uint32_t* claims;      // kClaimSlots chunk counters (bytes 128..255 of the same allocation), zero between calls
+    uint64_t call_seq;     // calls enqueued: call n uses claims[n % kClaimSlots]
     CUtensorMap tmap_k;    // 3-D tiled view of K: {head_dim, num_slots, kv_heads}, box {64, 64, 1}, 128B swizzle
     CUtensorMap tmap_v;
     int ctas_per_sm;       // resident attention CTAs per SM (occupancy)
@@ -54,6 +62,7 @@ struct Plan {
     int ctas;           // attention grid size C
     size_t off_len, off_row, off_prefix, off_unit_ok, off_po, off_plse;
     size_t off_sched;   // prompt attention: counter of claimed work units (zeroed by prep_kernel)
+    uint32_t* claim;    // decode attention: this call's chunk counter (reset by combine_kernel)
     size_t total;
 };
 

@@ -2,8 +2,9 @@
 //
 //   attn_kernel     persistent split-KV attention.  The work is the sequence
 //                   of (token, kv head, page) triples; each CTA streams an
-//                   equal slice of it, whatever the mix of row lengths.  A
-//                   producer warp streams the pages
+//                   equal slice of most of it, whatever the mix of row
+//                   lengths, then claims small chunks of the rest as it
+//                   finishes (split_of).  A producer warp streams the pages
 //                   through a shared-memory ring with TMA; four consumer warps
 //                   run QK^T and PV on mma.sync tensor cores with an online
 //                   softmax.  In decode mode the kernel also does the per-token
@@ -288,12 +289,16 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
 // Work order.  Tokens in order; within a token its kv heads; within a kv head
 // its pages 0..npg-1: unit u = t*G + g covers global pages
 // [G*pre[t] + g*npg[t], + npg[t]) with pre the exclusive prefix of npg over
-// tokens, T = G*sum(npg) pages in all.  CTA c of C' = min(C, T) streams the
-// slice [c*T/C', (c+1)*T/C'); CTAs beyond C' idle.  The piece of a unit inside
-// one slice is a segment.  A unit wholly inside one slice is written out
+// tokens, T = G*sum(npg) pages in all.  split_of cuts the sequence into
+// intervals: a static slice per CTA (CTAs beyond min(C, T) idle), then chunks
+// the CTAs claim from a counter as they finish.  The piece of a unit inside one
+// interval is a segment.  A unit wholly inside one interval is written out
 // directly; otherwise each piece leaves a partial (O/l and the base-2
-// log-sum-exp, for the 4 query heads) at index u + c -- unique, because units
-// and slices both increase along the sequence -- and combine_kernel merges them.
+// log-sum-exp, for the 4 query heads) at index u + i for interval i -- unique,
+// because units and intervals both increase along the sequence -- and
+// combine_kernel merges them in interval order, whichever CTA streamed each.
+// After its last range the producer sends a ring item without data that stops
+// the consumers.
 //
 // Per page, consumer warp w takes positions 16w..16w+15:
 //   QK^T:  S[16 pos][8 cols] = K_tile[16][128] * Qb[128][8]
@@ -373,8 +378,9 @@ struct AttnParams {
     __nv_bfloat16* K;         // pool
     __nv_bfloat16* V;
     __nv_bfloat16* out;       // [ntok][heads][128]
-    float* part_o;            // [U + C][4][128]
-    float* part_lse;          // [U + C][4]
+    float* part_o;            // [U + C (1 + kDynChunksPerCta)][4][128]
+    float* part_lse;          // [U + C (1 + kDynChunksPerCta)][4]
+    uint32_t* claim;          // chunk counter, zero at launch
     int32_t* prefix;          // [ntok + 1], written by CTA 0 for combine_kernel
     int32_t* unit_ok;         // [U], written by the CTA holding each unit's first page
     uint32_t* err;
@@ -395,7 +401,7 @@ constexpr int kSideBytes = 2560;
 constexpr int kSideQ = 0, kSideRopeHi = 1024, kSideRopeLo = 1536, kSideK = 2048, kSideV = 2304;
 
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagValid = 4, kFlagComplete = 8, kFlagHasLast = 16,
-              kFlagAppend = 32;
+              kFlagAppend = 32, kFlagStop = 64;
 
 template <int kStages>
 struct AttnSmem {
@@ -411,6 +417,57 @@ struct AttnSmem {
     static constexpr int kBytes = kFlag + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
 };
+
+// The work split.  Global pages [0, T) are cut into intervals: first Ce =
+// min(C, T) static slices of the first S pages, slice c = [c*S/Ce, (c+1)*S/Ce)
+// for CTA c; then, when there are two CTAs or more and at least
+// kDynMinPagesPerCta pages per CTA, a quarter of the pages in ND chunks of Q
+// pages, chunk k = [S + kQ, S + (k+1)Q),
+// which the CTAs claim from a counter once their slice is done.  The CTAs'
+// streaming rates differ by some 10-20% (the same pages take longer on some
+// SMs), so equal static slices alone end at different times; the chunks let
+// the fast CTAs take over the rest.  Q is 4 pages, or more where that keeps
+// ND <= kDynChunksPerCta * Ce (the partial slots of the workspace).
+constexpr int kDynMinPagesPerCta = 8;
+constexpr int kDynChunkPages = 4;
+
+struct Split {
+    int64_t S;  // pages in static slices
+    int Ce;     // static slices (CTAs with work)
+    int ND;     // chunks after them
+    int Q;      // pages per chunk
+};
+
+__device__ __forceinline__ Split split_of(int64_t T, int C)
+{
+    Split sp;
+    sp.Ce = (int)min((int64_t)C, T);
+    sp.S = T;
+    sp.ND = 0;
+    sp.Q = kDynChunkPages;
+    if (sp.Ce > 1 && T >= (int64_t)kDynMinPagesPerCta * sp.Ce) {
+        const int64_t dyn = T / 4, cap = (int64_t)kDynChunksPerCta * sp.Ce;
+        sp.Q = (int)max((int64_t)kDynChunkPages, (dyn + cap - 1) / cap);
+        sp.ND = (int)(dyn / sp.Q);
+        sp.S = T - (int64_t)sp.ND * sp.Q;
+    }
+    return sp;
+}
+
+// Slice c of C (C <= T) covers pages [c*T/C, (c+1)*T/C); the slice holding page x.
+__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int C)
+{
+    int c = (int)(x * C / T);
+    while (c + 1 < C && (int64_t)(c + 1) * T / C <= x) ++c;
+    while (c > 0 && (int64_t)c * T / C > x) --c;
+    return c;
+}
+
+// The interval (static slice or chunk) holding global page x < T.
+__device__ __forceinline__ int interval_of(int64_t x, const Split& sp)
+{
+    return x < sp.S ? cta_of(x, sp.S, sp.Ce) : sp.Ce + (int)((x - sp.S) / sp.Q);
+}
 
 __device__ __forceinline__ int npg_of(const AttnParams& p, int t)
 {
@@ -574,90 +631,114 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
     __syncthreads();
     const int64_t T = (int64_t)G * total;
-    const int Ce = (int)min((int64_t)C, T);  // never more slices than pages: none is empty
-    if (c >= Ce) return;
-    const int64_t gb = (int64_t)c * T / Ce, ge = (int64_t)(c + 1) * T / Ce;
+    const Split sp = split_of(T, C);  // never more slices than pages: none is empty
+    if (c >= sp.Ce) return;
 
     if (warp == kProducerWarp) {
         // ================================================================ producer
         int i = 0;  // ring items issued
         bool ok = true;
         const uint64_t pol = l2_policy_evict_first();
-        int t, pre;
-        find_token(p, sT0, sP0, gb, lane, t, pre);
-        int64_t St = (int64_t)G * pre;  // global index of (t, kv head 0, page 0)
-        int64_t x = gb;
-        while (x < ge && ok) {
-            const int n = npg_of(p, t);
-            const int64_t off = x - St;
-            const int g = (int)(off / n), j = (int)(off % n);
-            const int seg = (int)min((int64_t)(n - j), ge - x);
-            int row, len;
-            token_info(p, t, row, len);
-            const int pos = len - 1;
-            bool valid = true;
-            if (p.decode_mode) {  // every page the row will read must be a pool page
-                int bad = 0;
-                for (int q = lane; q < n; q += 32) {
-                    const int id = page_of(p.table, p.pages, row, q);
-                    bad |= (id < 0 || id >= p.num_pages);
+        // the static slice, then one claimed chunk after another; each claim is
+        // made when the range before it starts, so its answer is there at the end
+        int64_t xb = (int64_t)c * sp.S / sp.Ce, xe = (int64_t)(c + 1) * sp.S / sp.Ce;
+        int iv = c;  // the range's interval: partials of its pieces go to u + iv
+        uint32_t claim = 0;
+        if (sp.ND && lane == 0) claim = atomicAdd(p.claim, 1u);
+        for (;;) {
+            int t, pre;
+            find_token(p, sT0, sP0, xb, lane, t, pre);
+            int64_t St = (int64_t)G * pre;  // global index of (t, kv head 0, page 0)
+            int64_t x = xb;
+            while (x < xe && ok) {
+                const int n = npg_of(p, t);
+                const int64_t off = x - St;
+                const int g = (int)(off / n), j = (int)(off % n);
+                const int seg = (int)min((int64_t)(n - j), xe - x);
+                int row, len;
+                token_info(p, t, row, len);
+                const int pos = len - 1;
+                bool valid = true;
+                if (p.decode_mode) {  // every page the row will read must be a pool page
+                    int bad = 0;
+                    for (int q = lane; q < n; q += 32) {
+                        const int id = page_of(p.table, p.pages, row, q);
+                        bad |= (id < 0 || id >= p.num_pages);
+                    }
+                    valid = !__any_sync(kFull, bad);
                 }
-                valid = !__any_sync(kFull, bad);
-            }
-            const int u = t * G + g;
-            if (j == 0 && lane == 0) {
-                p.unit_ok[u] = valid ? 1 : 0;
-                if (!valid && g == 0) atomicOr(p.err, PKV_DEVERR_PAGE);
-            }
-            const bool has_last = j + seg == n;
-            const bool append = p.decode_mode && valid && has_last;
-            const int seg_flags = (valid ? kFlagValid : 0) | ((j == 0 && has_last) ? kFlagComplete : 0);
-            for (int s = 0; s < seg; ++s, ++i) {
-                const int jj = j + s, st = i % kStages;
-                if (i >= kStages && (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag)) {
-                    ok = false;
-                    break;
+                const int u = t * G + g;
+                if (j == 0 && lane == 0) {
+                    p.unit_ok[u] = valid ? 1 : 0;
+                    if (!valid && g == 0) atomicOr(p.err, PKV_DEVERR_PAGE);
                 }
-                int page = 0;
-                if (lane == 0 && valid) page = page_of(p.table, p.pages, row, jj);
-                page = __shfl_sync(kFull, page, 0);
-                if (lane == 0) {
-                    const int flags = seg_flags | (s == 0 ? kFlagFirst : 0) | (s == seg - 1 ? kFlagLast : 0) |
-                                      ((s == 0 && append) ? kFlagHasLast : 0) |
-                                      ((append && jj == n - 1) ? kFlagAppend : 0);
-                    sMeta[2 * st] = make_int4(t, g, jj, len);
-                    sMeta[2 * st + 1] = make_int4(flags, u + c, page, 0);
-                    const uint32_t fb = bar_full + 8 * st;
-                    const uint32_t dst = base + st * kStageBytes;
-                    uint32_t bytes = kStageBytes;
-                    if (s == 0) bytes += 1536 + (append ? 1024 : 0);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    const int y = page * kPageSize;
-                    tma_load_3d(dst, &tmK, 0, y, g, fb, pol);
-                    tma_load_3d(dst + 8192, &tmK, 64, y, g, fb, pol);
-                    tma_load_3d(dst + 16384, &tmV, 0, y, g, fb, pol);
-                    tma_load_3d(dst + 24576, &tmV, 64, y, g, fb, pol);
-                    if (s == 0) {
-                        const uint32_t side = base + L::kSide + st * kSideBytes;
-                        bulk_copy(side + kSideQ, p.q + ((int64_t)t * H + g * kGroup) * kHeadDim, 1024, fb);
-                        bulk_copy(side + kSideRopeHi, p.rope_hi + (int64_t)pos * kRopeHalf, 512, fb);
-                        if (append) {
-                            const int64_t kv = ((int64_t)t * G + g) * kHeadDim;
-                            bulk_copy(side + kSideRopeLo, p.rope_lo + (int64_t)pos * kRopeHalf, 512, fb);
-                            bulk_copy(side + kSideK, p.k + kv, 256, fb);
-                            bulk_copy(side + kSideV, p.v + kv, 256, fb);
+                const bool has_last = j + seg == n;
+                const bool append = p.decode_mode && valid && has_last;
+                const int seg_flags = (valid ? kFlagValid : 0) | ((j == 0 && has_last) ? kFlagComplete : 0);
+                for (int s = 0; s < seg; ++s, ++i) {
+                    const int jj = j + s, st = i % kStages;
+                    if (i >= kStages && (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    int page = 0;
+                    if (lane == 0 && valid) page = page_of(p.table, p.pages, row, jj);
+                    page = __shfl_sync(kFull, page, 0);
+                    if (lane == 0) {
+                        const int flags = seg_flags | (s == 0 ? kFlagFirst : 0) | (s == seg - 1 ? kFlagLast : 0) |
+                                          ((s == 0 && append) ? kFlagHasLast : 0) |
+                                          ((append && jj == n - 1) ? kFlagAppend : 0);
+                        sMeta[2 * st] = make_int4(t, g, jj, len);
+                        sMeta[2 * st + 1] = make_int4(flags, u + iv, page, 0);
+                        const uint32_t fb = bar_full + 8 * st;
+                        const uint32_t dst = base + st * kStageBytes;
+                        uint32_t bytes = kStageBytes;
+                        if (s == 0) bytes += 1536 + (append ? 1024 : 0);
+                        mbar_arrive_expect_tx(fb, bytes);
+                        const int y = page * kPageSize;
+                        tma_load_3d(dst, &tmK, 0, y, g, fb, pol);
+                        tma_load_3d(dst + 8192, &tmK, 64, y, g, fb, pol);
+                        tma_load_3d(dst + 16384, &tmV, 0, y, g, fb, pol);
+                        tma_load_3d(dst + 24576, &tmV, 64, y, g, fb, pol);
+                        if (s == 0) {
+                            const uint32_t side = base + L::kSide + st * kSideBytes;
+                            bulk_copy(side + kSideQ, p.q + ((int64_t)t * H + g * kGroup) * kHeadDim, 1024, fb);
+                            bulk_copy(side + kSideRopeHi, p.rope_hi + (int64_t)pos * kRopeHalf, 512, fb);
+                            if (append) {
+                                const int64_t kv = ((int64_t)t * G + g) * kHeadDim;
+                                bulk_copy(side + kSideRopeLo, p.rope_lo + (int64_t)pos * kRopeHalf, 512, fb);
+                                bulk_copy(side + kSideK, p.k + kv, 256, fb);
+                                bulk_copy(side + kSideV, p.v + kv, 256, fb);
+                            }
                         }
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
+                x += seg;
+                if (ok && x < xe && x >= St + (int64_t)G * n) {  // next token that has pages
+                    St += (int64_t)G * n;
+                    do {
+                        ++t;
+                    } while (npg_of(p, t) == 0);
+                }
             }
-            x += seg;
-            if (ok && x < ge && x >= St + (int64_t)G * n) {  // next token that has pages
-                St += (int64_t)G * n;
-                do {
-                    ++t;
-                } while (npg_of(p, t) == 0);
+            if (!ok || !sp.ND) break;
+            const uint32_t k = __shfl_sync(kFull, claim, 0);
+            if (k >= (uint32_t)sp.ND) break;
+            if (lane == 0) claim = atomicAdd(p.claim, 1u);
+            xb = sp.S + (int64_t)k * sp.Q;
+            xe = xb + sp.Q;
+            iv = sp.Ce + (int)k;
+        }
+        if (ok) {  // the end: a ring item without data that stops the consumers
+            const int st = i % kStages;
+            if (i >= kStages && (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag)) {
+                ok = false;
+            } else if (lane == 0) {
+                sMeta[2 * st + 1] = make_int4(kFlagStop, 0, 0, 0);
+                mbar_arrive(bar_full + 8 * st);
             }
+            __syncwarp();
         }
         if (!ok && lane == 0) {
             atomicOr(p.err, PKV_DEVERR_TIMEOUT);
@@ -698,8 +779,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     uint2 knew = make_uint2(0u, 0u), vnew = make_uint2(0u, 0u);  // the row's new k (normed, roped) and v
     bool ok = true;
 
-    const int nitems = (int)(ge - gb);
-    for (int i = 0; i < nitems; ++i) {
+    for (int i = 0;; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
             ok = false;
@@ -707,6 +787,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
         const int4 m1 = sMeta[2 * st + 1];
         const int flags = m1.x;
+        if (flags & kFlagStop) break;
         const int4 m0 = sMeta[2 * st];
         const int t = m0.x, g = m0.y, jj = m0.z, len = m0.w, pidx = m1.y, page = m1.z;
         const uint32_t kb = base + st * kStageBytes;
@@ -981,6 +1062,7 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.part_o = reinterpret_cast<float*>(a.ws + plan.off_po);
     p.part_lse = reinterpret_cast<float*>(a.ws + plan.off_plse);
+    p.claim = plan.claim;
     p.prefix = reinterpret_cast<int32_t*>(a.ws + plan.off_prefix);
     p.unit_ok = reinterpret_cast<int32_t*>(a.ws + plan.off_unit_ok);
     p.err = pool->err;
@@ -1019,17 +1101,9 @@ struct CombineParams {
     const float* part_lse;
     __nv_bfloat16* out;
     uint32_t* err;
+    uint32_t* claim;          // the attention's chunk counter: zeroed here for the call that next uses it
     int ntok, heads, kv_heads, ctas, decode_mode;
 };
-
-// CTA c of C (C <= T) covers global pages [c*T/C, (c+1)*T/C); the CTA holding page x.
-__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int C)
-{
-    int c = (int)(x * C / T);
-    while (c + 1 < C && (int64_t)(c + 1) * T / C <= x) ++c;
-    while (c > 0 && (int64_t)c * T / C > x) --c;
-    return c;
-}
 
 // One CTA per (token, kv head) unit; warp w = query head 4g+w, lane owns dims 4*lane..4*lane+3.
 //   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M)   over the unit's pieces c
@@ -1041,9 +1115,12 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
     const int t = u / G, g = u % G;
     const int h = g * kGroup + warp;
     pdl_wait();
+    if (u == 0 && threadIdx.x == 0) *p.claim = 0;  // the attention grid has finished claiming
     __nv_bfloat16* dst = p.out + ((int64_t)t * p.heads + h) * kHeadDim + 4 * lane;
-    const int pre = p.prefix[t];
-    const int n = p.prefix[t + 1] - pre;
+    // every index this CTA needs, loaded together (one round trip)
+    const int pre = p.prefix[t], pre1 = p.prefix[t + 1], total = p.prefix[p.ntok];
+    const int uok = p.unit_ok[u];
+    const int n = pre1 - pre;
     if (n == 0) {  // skipped token
         *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
         if (p.decode_mode && g == 0 && threadIdx.x == 0) {
@@ -1052,29 +1129,56 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
         }
         return;
     }
-    if (!p.unit_ok[u]) {
+    if (!uok) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
         return;
     }
-    const int64_t T = (int64_t)G * p.prefix[p.ntok];
-    const int Ce = (int)min((int64_t)p.ctas, T);  // the slices the attention kernel used
+    const int64_t T = (int64_t)G * total;
+    const Split sp = split_of(T, p.ctas);  // the attention kernel's intervals
     const int64_t S = (int64_t)G * pre + (int64_t)g * n;
-    const int64_t rf = cta_of(S, T, Ce), rl = cta_of(S + n - 1, T, Ce);
-    if (rf == rl) return;  // one CTA held the whole unit and wrote it out
-    float M = -CUDART_INF_F;
-    for (int64_t r = rf + lane; r <= rl; r += 32) M = fmaxf(M, p.part_lse[((int64_t)u + r) * kGroup + warp]);
+    const int64_t rf = interval_of(S, sp), rl = interval_of(S + n - 1, sp);
+    if (rf == rl) return;  // one interval held the whole unit, and its CTA wrote it out
+    // the pieces' log-sum-exps, one per lane, and the first kPre pieces' partial
+    // outputs, all in flight together (a second round trip); then the rest of
+    // the outputs in piece order, batches of independent loads
+    constexpr int kPre = 4;
+    const int np = (int)(rl - rf + 1);
+    const float* lse = p.part_lse + ((int64_t)u + rf) * kGroup + warp;
+    const float* po = p.part_o + (((int64_t)u + rf) * kGroup + warp) * kHeadDim + 4 * lane;
+    const int64_t ostride = (int64_t)kGroup * kHeadDim;
+    const float l0 = lane < np ? lse[(int64_t)lane * kGroup] : -CUDART_INF_F;
+    float4 ob[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k)
+        ob[k] = k < np ? *reinterpret_cast<const float4*>(po + k * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = l0;
+    for (int r = lane + 32; r < np; r += 32) M = fmaxf(M, lse[(int64_t)r * kGroup]);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+    const float wl0 = lane < np ? exp2f(l0 - M) : 0.f;
     float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int64_t r = rf; r <= rl; ++r) {
-        const int64_t ph = ((int64_t)u + r) * kGroup + warp;
-        const float w = exp2f(p.part_lse[ph] - M);
-        const float4 o = *reinterpret_cast<const float4*>(p.part_o + ph * kHeadDim + 4 * lane);
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {  // pieces beyond np add w = 0 times o = 0
+        const float w = __shfl_sync(kFull, wl0, k);
         wsum += w;
-        acc[0] += w * o.x;
-        acc[1] += w * o.y;
-        acc[2] += w * o.z;
-        acc[3] += w * o.w;
+        acc[0] += w * ob[k].x;
+        acc[1] += w * ob[k].y;
+        acc[2] += w * ob[k].z;
+        acc[3] += w * ob[k].w;
+    }
+    for (int r0 = 0; r0 < np; r0 += 32) {
+        const int nb = min(32, np - r0);
+        const float wl = r0 == 0 ? wl0 : (lane < nb ? exp2f(lse[(int64_t)(r0 + lane) * kGroup] - M) : 0.f);
+#pragma unroll 4
+        for (int r = r0 == 0 ? kPre : 0; r < nb; ++r) {
+            const float w = __shfl_sync(kFull, wl, r);
+            const float4 o = *reinterpret_cast<const float4*>(po + (r0 + r) * ostride);
+            wsum += w;
+            acc[0] += w * o.x;
+            acc[1] += w * o.y;
+            acc[2] += w * o.z;
+            acc[3] += w * o.w;
+        }
     }
     const float inv = 1.f / wsum;
     const float y[4] = {acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv};
@@ -1090,6 +1194,7 @@ cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.positions = a.step_positions;
     p.part_o = reinterpret_cast<const float*>(a.ws + plan.off_po);
     p.part_lse = reinterpret_cast<const float*>(a.ws + plan.off_plse);
+    p.claim = plan.claim;
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.err = pool->err;
     p.ntok = plan.tokens;
