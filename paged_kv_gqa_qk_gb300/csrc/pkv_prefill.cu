@@ -524,7 +524,8 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int b = 0; b < nb; ++b) {
                 const int j = it + b;
-                if (!mbar_wait_spin(c.bar_s + 8 * h, j & 1) || *c.abort_flag) {
+                // every exit decision is warp-wide: the tensor-memory accesses below are
+                if (__any_sync(kAll, !mbar_wait_spin(c.bar_s + 8 * h, j & 1) || *c.abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -568,7 +569,7 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
                 }
                 if (__any_sync(kAll, need)) {
                     // O must hold the previous block's product first
-                    if (!mbar_wait_spin(c.bar_o + 8 * h, (j - 1) & 1)) {
+                    if (__any_sync(kAll, !mbar_wait_spin(c.bar_o + 8 * h, (j - 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -616,7 +617,7 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
             }
             if (!ok) break;
             // ---- epilogue of this row's pass: O / l for the active rows
-            if (!mbar_wait_spin(c.bar_o + 8 * h, (it + nb - 1) & 1)) {
+            if (__any_sync(kAll, !mbar_wait_spin(c.bar_o + 8 * h, (it + nb - 1) & 1))) {
                 ok = false;
                 break;
             }
