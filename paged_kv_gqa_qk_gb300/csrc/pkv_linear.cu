@@ -67,6 +67,53 @@ __device__ __forceinline__ __nv_bfloat16* seg_of(const LinParams& p, int m0, int
     return p.y[s];
 }
 
+// Split-K epilogue of one CTA of a cluster of NS: sum its groups of four features
+// [r * 32 / NS, (r + 1) * 32 / NS) of the tile over the NS partial tiles ([token][feature]
+// fp32 in each CTA's shared memory at `local`), in rank order, and write them to y.  A
+// thread issues the loads of up to 16 float4 (several items, every source) before the
+// first sum, so the remote reads cost about one round trip rather than one per item.
+template <int BN, int NS>
+__device__ __forceinline__ void cluster_reduce(uint32_t local, int r, int tid, int n0, int tokens,
+                                               __nv_bfloat16* y, int yw, int yc)
+{
+    constexpr int kPer = (kBM / 4) / NS;  // groups of four features per CTA
+    constexpr int kPerThread = BN * kPer / kLinThreads;
+    constexpr int R = (16 / NS) < kPerThread ? (16 / NS) : kPerThread;  // items per round
+    static_assert(kPerThread % R == 0, "whole rounds");
+    uint32_t src[NS];
+#pragma unroll
+    for (int q = 0; q < NS; ++q) src[q] = cluster_map(local, q);
+#pragma unroll 1
+    for (int r0 = 0; r0 < kPerThread; r0 += R) {
+        float4 v[R][NS];
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int idx = tid + kLinThreads * (r0 + u), t = idx / kPer, f = 4 * (r * kPer + idx % kPer);
+            const uint32_t off = (uint32_t)(t * kBM + f) * 4;
+#pragma unroll
+            for (int q = 0; q < NS; ++q) v[u][q] = ld_cluster_f32x4(src[q] + off);
+        }
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int idx = tid + kLinThreads * (r0 + u), t = idx / kPer, f = 4 * (r * kPer + idx % kPer);
+            float4 acc = v[u][0];
+#pragma unroll
+            for (int q = 1; q < NS; ++q) {
+                acc.x += v[u][q].x;
+                acc.y += v[u][q].y;
+                acc.z += v[u][q].z;
+                acc.w += v[u][q].w;
+            }
+            if (n0 + t < tokens) {
+                uint2 o2;
+                o2.x = pack_bf16(__float2bfloat16_rn(acc.x), __float2bfloat16_rn(acc.y));
+                o2.y = pack_bf16(__float2bfloat16_rn(acc.z), __float2bfloat16_rn(acc.w));
+                *reinterpret_cast<uint2*>(y + (int64_t)(n0 + t) * yw + yc + f) = o2;
+            }
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
     linear_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, LinParams p)
@@ -191,30 +238,12 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
         tc_fence_after();
         tmem_dealloc(tmem, BN);
     }
-    // CTA r sums features [r * 128 / ns, (r + 1) * 128 / ns) of the tile over the ns CTAs, in
-    // rank order, four features (16 bytes) at a time
-    const int ns = p.splits, per4 = kBM / ns / 4, r = (int)cluster_rank();
     const uint32_t local = smem_u32(part);
-    for (int idx = tid; idx < BN * per4; idx += kLinThreads) {
-        const int t = idx / per4, f = r * (kBM / ns) + 4 * (idx % per4);
-        const uint32_t off = (uint32_t)(t * kBM + f) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < kMaxSplits; ++q) {
-            if (q < ns) {
-                const float4 v = ld_cluster_f32x4(cluster_map(local + off, q));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-        }
-        if (n0 + t < p.tokens) {
-            uint2 o2;
-            o2.x = pack_bf16(__float2bfloat16_rn(acc.x), __float2bfloat16_rn(acc.y));
-            o2.y = pack_bf16(__float2bfloat16_rn(acc.z), __float2bfloat16_rn(acc.w));
-            *reinterpret_cast<uint2*>(y + (int64_t)(n0 + t) * yw + yc + f) = o2;
-        }
+    const int r = (int)cluster_rank();
+    switch (p.splits) {  // linear_splits gives 2, 4 or 8
+    case 2: cluster_reduce<BN, 2>(local, r, tid, n0, p.tokens, y, yw, yc); break;
+    case 4: cluster_reduce<BN, 4>(local, r, tid, n0, p.tokens, y, yw, yc); break;
+    default: cluster_reduce<BN, 8>(local, r, tid, n0, p.tokens, y, yw, yc); break;
     }
     cluster_sync();  // no CTA leaves while another reads its shared memory
 }

@@ -46,6 +46,7 @@ def pool():
     (7, 256, 384),        # ragged token tile, 3 output tiles
     (64, 4096, 1024),     # k_proj / v_proj of the 64-row decode batch (split over the input features)
     (64, 4096, 4096),     # q_proj / o_proj of the same batch
+    (64, 4096, 6144),     # q, k, v stacked for the same batch (a cluster of 6: uneven feature slices)
     (200, 512, 640),      # a 256-token tile with a ragged tail
     (300, 1024, 256),     # two token tiles, the second ragged
 ])
