@@ -17,10 +17,10 @@
  *   4. attends: query head h reads kv head h / (heads / kv_heads) over the
  *      row's positions 0..pos inclusive, scale 1/sqrt(head_dim)
  *      (decode_paged's paged_attention; decode_rows' mask s <= positions[b]).
- * The q/k/v projections before and the output projection after are not part
- * of this library: callers pass the projected q, k, v split into heads
- * (split_heads: [tokens][heads][head_dim]) and receive the attention output in
- * the same layout (merge_heads of it is a reshape).
+ * The attention entries take the projected q, k, v split into heads
+ * (split_heads: [tokens][heads][head_dim]) and return the attention output in
+ * the same layout (merge_heads of it is a reshape).  The projections around
+ * them are separate entries (pkv_qkv_proj before, pkv_linear for o_proj).
  *
  * Conventions shared by every entry point.
  *   - bf16 tensors are passed as void pointers to IEEE bfloat16 data.
@@ -45,6 +45,10 @@
  *     table[rows[p]][positions[p] / page_size] * page_size + positions[p] % page_size.
  *     Tokens the device checks would skip take no part.  The check is for
  *     debugging: it synchronises, so it does not belong in a captured graph.
+ *   - Calls on one pool may run concurrently on different streams as long as
+ *     they write different slots.  Each pkv_decode / pkv_step call takes one
+ *     of the pool's 32 work counters in turn (zero between calls), so at most
+ *     32 such calls may be in flight at once.
  *   - Every `table` argument may be NULL: the contiguous-row layout of the
  *     pages' non-paged entries (src/attention.linnet decode_rows,
  *     prefill_packed, step_packed), where row b owns the `pages` pool pages
@@ -160,8 +164,8 @@ PKV_API int pkv_pool_kv(const pkv_pool* pool, void** k, void** v, int64_t* num_s
  * aligned) and passes it to pkv_decode / pkv_step / pkv_prefill; its contents need no
  * initialisation and are not meaningful after the call.  The size depends
  * only on the pool (its config and attention grid size, see pkv_set_ctas),
- * rows and prefill_tokens: about 16.5 KiB per token plus 2 KiB per attention
- * CTA.
+ * rows and prefill_tokens: about 16.5 KiB per token plus 35 KiB per attention
+ * CTA (room for the partial results of the pieces the work split makes).
  * Errors: PKV_EINVAL (null, rows < 0, prefill_tokens < 0, both zero,
  * pages <= 0), PKV_ERANGE (more than 2^20 tokens). */
 PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_tokens, size_t* bytes);
@@ -338,9 +342,12 @@ PKV_API int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags);
 
 /* ---- tuning and measurement ---------------------------------------------------------------
  * Grid size of the attention kernel (0 = one wave: every SM's resident
- * CTAs).  The kernel splits the call's (token, kv head, page) sequence into
- * that many equal slices; results do not depend on it beyond floating-point
- * association.  It changes pkv_workspace_bytes.  Errors: PKV_EINVAL (null, < 0). */
+ * CTAs).  The kernel cuts the call's (token, kv head, page) sequence into
+ * that many equal slices of about three quarters of it, one per CTA, and
+ * chunks of 4+ pages of the rest that the CTAs claim as they finish (with one
+ * CTA, a single slice).  Results are reproducible run to run and do not
+ * depend on the grid size beyond floating-point association.  It changes
+ * pkv_workspace_bytes.  Errors: PKV_EINVAL (null, < 0). */
 PKV_API int pkv_set_ctas(pkv_pool* pool, int ctas);
 
 /* Kernel timer: while enabled, every pkv_decode / pkv_step records a pair of
