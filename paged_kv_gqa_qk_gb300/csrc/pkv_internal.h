@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pkv.h"
 
 namespace pkv {
@@ -41,7 +43,7 @@ struct pkv_pool {
     float2* rope_lo;       // the double values minus rope_hi, in fp32
     uint32_t* err;         // sticky device error word (word 0 of a 256-byte allocation)
     uint32_t* claims;      // kClaimSlots chunk counters (bytes 128..255 of the same allocation), zero between calls
-    uint64_t call_seq;     // calls enqueued: call n uses claims[n % kClaimSlots]
+    std::atomic<uint64_t> call_seq;  // calls enqueued (from any host thread): call n uses claims[n % kClaimSlots]
     CUtensorMap tmap_k;    // 3-D tiled view of K: {head_dim, num_slots, kv_heads}, box {64, 64, 1}, 128B swizzle
     CUtensorMap tmap_v;
     int ctas_per_sm;       // resident attention CTAs per SM (occupancy)
