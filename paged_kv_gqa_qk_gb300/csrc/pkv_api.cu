@@ -98,7 +98,11 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
         if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
         pool->timer_count++;
     }
-    if (launch_combine(pool, as, ps, decode, s) != cudaSuccess) return PKV_ECUDA;
+    if (launch_combine(pool, as, ps, decode, s) != cudaSuccess) {
+        // the combine resets this call's chunk counter; without it, reset it here
+        cudaMemsetAsync(ps.claim, 0, sizeof(uint32_t), s);
+        return PKV_ECUDA;
+    }
     return PKV_OK;
 }
 
