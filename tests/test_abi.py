@@ -96,3 +96,16 @@ def test_no_device_is_reported(lib):
     out = ctypes.c_void_p()
     cfg = pkv.pkv_config_default()
     assert lib.pkv_pool_alloc(ctypes.byref(cfg), 8, None, ctypes.byref(out)) == pkv.PKV_EDEVICE
+
+
+def test_missing_library_fails_loudly():
+    """No CPU fallback: without libpkv.so the binding raises instead of computing anything."""
+    p = subprocess.run(
+        [__import__("sys").executable, "-c",
+         "import paged_kv_gqa_qk_gb300 as pkv\n"
+         "try:\n"
+         "    pkv.load_library('/nonexistent/libpkv.so')\n"
+         "except RuntimeError as e:\n"
+         "    print('raised', e)\n"],
+        cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert p.returncode == 0 and p.stdout.startswith("raised") and "libpkv.so not found" in p.stdout
