@@ -2,14 +2,20 @@
 
 One step = one pkv_decode call over a batch: QK-norm + RoPE + KV append for
 every row, split-KV attention over each row's pages, and the split combine.
-The default workload is 64 rows with context lengths U[512, 4096] at
-Qwen3-8B attention shapes (32 query heads, 8 kv heads, head_dim 128, pages of
-64), synthetic and seeded.  Metric: decode rows/s (and the KV-read GB/s it
-implies), with the attention kernel's achieved HBM bandwidth against the
-measured copy bandwidth of the chip.
+The default workload is the largest single-GPU decode batch: 256 rows with
+context lengths U[1024, 8192], in groups of 16 rows that share their first
+8-32 pages (a shared prompt prefix), at Qwen3-8B attention shapes (32 query
+heads, 8 kv heads, head_dim 128, pages of 64), synthetic and seeded.
+Metric: decode rows/s (and the KV-read GB/s it implies, logical and unique),
+with the attention kernel's achieved HBM bandwidth on unique bytes against
+the measured copy bandwidth of the chip.  After the K timed steps the same
+step runs back to back for a few seconds (the sustained pass) while the SM
+clocks are sampled, and its median per-step time is reported beside
+ms_per_step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload config2|config3|config4|config5|sweepRxL|prefill|rows|linear_decode|linear_prefill]
+                  [--workload config4|config2|config3|config5|sweepRxL|prefill|rows|linear_decode|linear_prefill]
+                  [--sustain-seconds S]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch of the
@@ -21,6 +27,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -36,6 +43,16 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 126 << 20          # L2 of one GB300 as the driver reports it
 L2_FLUSH_BYTES = 512 << 20
+L2_CLEAN_BYTES = 256 << 20
+
+
+def l2_flush(write_buf, read_buf):
+    """Evict the step's inputs from L2: write a buffer larger than L2, then
+    read another one, so that L2 is left holding clean lines (a kernel that
+    follows pays no write-back of the flush's own dirty lines)."""
+    import torch
+    write_buf.zero_()
+    torch.sum(read_buf)
 
 
 # ---------------------------------------------------------------------------- distributed helpers
@@ -100,7 +117,7 @@ def make_workload(name: str, rank: int = 0):
 # ---------------------------------------------------------------------------- measurement helpers
 
 class ClockSampler:
-    """nvidia-smi SM clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi SM clocks and throttle reasons sampled every 100 ms while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -112,7 +129,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -210,22 +227,62 @@ def prefill_algorithmic_flops(wl) -> int:
     return sum(4 * H * D * (int(p) + 1) for p in wl.positions.tolist())
 
 
-def attention_algorithmic_bytes(wl) -> int:
+def attention_algorithmic_bytes(wl, unique: bool = True) -> int:
     """Bytes the decode attention kernel must move per launch: K and V of every
     attended position (4096 B each at 8 kv heads x 128 x bf16 x 2), and per
     row its page-table entries, its q (bf16, read), its new k and v (bf16,
-    read, then written to the pool) and its bf16 output."""
+    read, then written to the pool) and its bf16 output.  unique: a page that
+    several rows share (a shared prefix) counts once."""
     import workloads as W
     S = wl.cfg["page_size"]
     L = [int(p) + 1 for p in wl.step_positions.tolist() if p >= 0]  # the rows the attention kernel serves
     kv = W.kv_bytes_per_position(wl.cfg) * sum(L)
-    if wl.meta.get("unique_kv_bytes") and wl.kind == "decode":
+    if unique and wl.meta.get("unique_kv_bytes") and wl.kind == "decode":
         # rows sharing prefix pages: each shared page counts once (later reads are L2 hits)
         kv = min(kv, wl.meta["unique_kv_bytes"])
     table = 4 * sum(-(-x // S) for x in L)
     H, G, D = wl.cfg["heads"], wl.cfg["kv_heads"], wl.cfg["head_dim"]
     per_row = 2 * (H * D + 2 * G * D + 2 * G * D + H * D)
     return kv + table + len(L) * per_row
+
+
+def sustained_pass(step, flush, stream, ms_step_hint: float, seconds: float, block: int = 16) -> dict:
+    """The same step back to back for about `seconds` (at least one block),
+    timed with CUDA events on the launching stream: one pair per block of
+    `block` steps when the inputs exceed L2, else one pair around each step
+    with an L2 flush before it (outside the pair).  Returns the median and
+    mean per-step time and the wall time the pass took."""
+    import torch
+    if seconds <= 0:
+        return {"seconds": 0.0, "steps": 0}
+    n = max(block, int(math.ceil(seconds * 1e3 / max(ms_step_hint, 1e-3))))
+    n = (n + block - 1) // block * block
+    per_step = []
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        if flush is None:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n // block + 1)]
+            evs[0].record(stream)
+            for b in range(n // block):
+                for _ in range(block):
+                    step()
+                evs[b + 1].record(stream)
+            stream.synchronize()
+            per_step = [evs[b].elapsed_time(evs[b + 1]) / block for b in range(n // block)]
+        else:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+            for i in range(n):
+                flush()
+                evs[2 * i].record(stream)
+                step()
+                evs[2 * i + 1].record(stream)
+            stream.synchronize()
+            per_step = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(n)]
+    wall = time.perf_counter() - t0
+    return {"seconds": wall, "steps": n, "ms_per_step_median": statistics.median(per_step),
+            "ms_per_step_mean": sum(per_step) / len(per_step),
+            "timing": (f"CUDA events every {block} steps, back to back" if flush is None else
+                       "CUDA events around each step, L2 flushed before each (outside the events)")}
 
 
 # ---------------------------------------------------------------------------- the GPU arm
@@ -292,11 +349,12 @@ def run_gpu(args) -> None:
     # the timed events) before every timed step.
     logical = wl.meta["logical_kv_bytes"]
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if logical < 2 * L2_BYTES else None
+    clean_buf = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev) if flush_buf is not None else None
 
     def flush():
         if flush_buf is not None:
             with torch.cuda.stream(stream):
-                flush_buf.zero_()
+                l2_flush(flush_buf, clean_buf)
 
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 if flush_buf is None else 2 * args.steps)]
     barrier(world)
@@ -320,10 +378,13 @@ def run_gpu(args) -> None:
             flush()
             step()
         torch.cuda.synchronize()
+        attn_ms, attn_n = pkv.pkv_timer_read(pool.handle)
+        pkv.pkv_timer_enable(pool.handle, False)
+        ms_first = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(len(evs) // 2)) / args.steps
+        sustained = sustained_pass(step, flush if flush_buf is not None else None, stream, ms_first,
+                                   args.sustain_seconds)
     barrier(world)
     ms_total = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(len(evs) // 2))
-    attn_ms, attn_n = pkv.pkv_timer_read(pool.handle)
-    pkv.pkv_timer_enable(pool.handle, False)
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
 
@@ -374,11 +435,18 @@ def run_gpu(args) -> None:
         plan_bytes = attention_algorithmic_bytes(wl)
         achieved = plan_bytes / attn_avg_s / 1e9
         peak, peak_kind = measured_peak_hbm()
+        logical_bytes = attention_algorithmic_bytes(wl, unique=False)
         roofline = {"bound": "hbm", "kernel": "attn_kernel", "achieved": achieved, "peak": peak,
                     "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
                     "traffic": ncu_traffic(args.workload), "algorithmic_bytes_per_launch": plan_bytes,
+                    "bytes_counted": ("unique: each shared prefix page once" if logical_bytes != plan_bytes
+                                      else "every attended position"),
+                    "achieved_logical": logical_bytes / attn_avg_s / 1e9,
                     "avg_launch_us": attn_avg_s * 1e6, "timed_launches": attn_n, "timing": timing}
-    rows_total = ntok * world  # tokens attended per step (decode: rows)
+    # value: decode rows per second (a step's prompt tokens are reported beside it);
+    # a prefill-only call has no decode rows and reports prompt tokens per second
+    n_decode = int((wl.step_positions >= 0).sum()) if wl.kind != "prefill" else 0
+    rows_total = (P if wl.kind == "prefill" else n_decode) * world
     unit = "tokens/s" if wl.kind == "prefill" else "rows/s"
     res = {
         "metric": METRIC,
@@ -401,7 +469,8 @@ def run_gpu(args) -> None:
                    "kv_bytes_per_step": logical,
                    "l2": (f"inputs larger than L2: {logical / 1e9:.2f} GB of K/V per step vs 126 MB L2"
                           if flush_buf is None else
-                          f"L2 flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the "
+                          f"L2 flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, then a "
+                          f"{L2_CLEAN_BYTES >> 20} MiB read so that L2 holds clean lines; outside the "
                           f"device-timed events, inside the e2e time): {logical / 1e6:.0f} MB of K/V per step"),
                    "parallelism": f"dp{world} (independent replicas, rows sharded by rank)"},
         "kv_gbs": logical / (ms_step / 1e3) / 1e9 * world,
@@ -411,7 +480,11 @@ def run_gpu(args) -> None:
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
+        "sustained": sustained,
     }
+    if wl.kind == "step":
+        res["prompt_tokens_per_s"] = P * world / (ms_step / 1e3)
+        res["config"]["decode_rows"] = n_decode
     if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.kind == "decode":
         res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     pool.close()
@@ -465,10 +538,11 @@ def run_gpu_linear(args) -> None:
             step()
     stream.synchronize()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)  # the weights (84 MB) fit in L2
+    clean_buf = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
 
     def flush():
         with torch.cuda.stream(stream):
-            flush_buf.zero_()
+            l2_flush(flush_buf, clean_buf)
 
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
     barrier(world)
@@ -544,8 +618,9 @@ def run_gpu_linear(args) -> None:
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,1/4096) bf16 weights)",
         "config": {"workload": f"projections q/k/v/o of one layer, {tokens} tokens, hidden 4096",
                    "tokens": tokens, "shapes": [list(s) for s in LINEAR_SHAPES],
-                   "l2": f"L2 flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the "
-                         f"device-timed events, inside the e2e time): {weight_bytes / 1e6:.0f} MB of weights",
+                   "l2": f"L2 flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, then a "
+                      f"{L2_CLEAN_BYTES >> 20} MiB read so that L2 holds clean lines; outside the device-timed "
+                      f"events, inside the e2e time): {weight_bytes / 1e6:.0f} MB of weights",
                    "parallelism": f"dp{world} (independent replicas)"},
         "roofline": roofline,
         "e2e": {"value": tokens * args.steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -652,7 +727,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
-    ap.add_argument("--workload", default="config2")
+    ap.add_argument("--workload", default="config4")
+    ap.add_argument("--sustain-seconds", type=float, default=2.0,
+                    help="length of the back-to-back pass after the timed steps (0: none)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

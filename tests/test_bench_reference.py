@@ -30,7 +30,8 @@ def test_reference_arm_prints_one_contract_line():
     assert d["unit"] == "rows/s" and d["higher_is_better"] is True and d["scaling"] == "weak"
     assert (d["n_gpus"], d["steps"], d["warmup"]) == (1, 1, 3)
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
-    assert d["config"]["workload"] == "decode 64 rows x U[512,4096]"
+    # the default workload: the largest single-GPU decode batch (shared prefixes)
+    assert d["config"]["workload"].startswith("shared-prefix decode 256 rows x U[1024,8192]")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e2e = d["e2e"]
@@ -44,7 +45,7 @@ def test_reference_arm_under_two_ranks_prints_from_rank_0_only():
         port = s.getsockname()[1]
     p = _run(["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
               "--master-port", str(port), "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
-              "--warmup", "3"])
+              "--warmup", "3", "--workload", "config2"])
     assert p.returncode == 0, p.stderr[-2000:]
     lines = _json_lines(p.stdout)
     assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
