@@ -461,3 +461,39 @@ def test_invalid_tokens_are_skipped_with_error_bits():
     pos2[1] = -1
     out2, err2 = oracle.decode(K2, V2, *args, pos2, wl.table.numpy())
     assert err2 == 0 and not out2[1].any()
+
+
+def test_explicit_slot_outside_the_pool_is_skipped():
+    """The slot-check branch of the step: a prompt token whose explicit slot
+    lies outside the pool (negative, or num_slots and beyond) is skipped with
+    ERR_SLOT -- no write, zero output -- and nothing else changes.  The bad
+    tokens are the last of their prompts, so no other token reads the slots
+    they would have written: every other output, and the whole pool except
+    those two slots, must equal the call with the correct slots."""
+    cfg = dict(CFG)
+    wl = W.make_step("slot errors", prompt_lengths=[70, 5], prompt_starts=[60, 0], decode_lengths=[90, 3],
+                     seed=16, table_pages=3)
+    args = [W.bits(t) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w)]
+    pos, prow, sp, table = (wl.positions.numpy(), wl.prow.numpy(), wl.step_positions.numpy(), wl.table.numpy())
+    slots = oracle.page_slots(table, prow, pos)
+    K, V = W.bits(wl.K0).copy(), W.bits(wl.V0).copy()
+    ref, err = oracle.step(K, V, *args, pos, prow, slots, sp, table, cfg=cfg)
+    assert err == 0
+    num_slots = K.shape[1]
+    bad = slots.copy()
+    last0, last1 = 69, 74                   # last token of each prompt
+    bad[last0] = num_slots                  # one past the pool
+    bad[last1] = -3                         # negative
+    Kb, Vb = W.bits(wl.K0).copy(), W.bits(wl.V0).copy()
+    out, errb = oracle.step(Kb, Vb, *args, pos, prow, bad, sp, table, cfg=cfg)
+    assert errb == oracle.ERR_SLOT
+    assert not out[last0].any() and not out[last1].any()
+    keep = np.ones(out.shape[0], dtype=bool)
+    keep[[last0, last1]] = False
+    np.testing.assert_array_equal(out[keep], ref[keep])
+    # the pool: the two skipped tokens' slots keep their old contents, all else as the good call left it
+    K0, V0 = W.bits(wl.K0), W.bits(wl.V0)
+    for s in (slots[last0], slots[last1]):
+        assert np.array_equal(Kb[:, s], K0[:, s]) and np.array_equal(Vb[:, s], V0[:, s])
+        Kb[:, s], Vb[:, s] = K[:, s], V[:, s]
+    assert np.array_equal(Kb, K) and np.array_equal(Vb, V)
