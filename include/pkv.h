@@ -38,13 +38,16 @@
  *     in the pool's sticky error word, read with pkv_check_errors().  No
  *     kernel traps or spins without bound.
  *   - Optional host pre-check: with the environment variable PKV_CHECK=1,
- *     pkv_decode, pkv_step and pkv_prefill first synchronise the stream, copy
- *     the call's positions, rows, slots and table to the host and return
- *     PKV_EINVAL (nothing enqueued) when two written slots coincide outside
- *     pool page 0, or when a given prompt slot differs from
- *     table[rows[p]][positions[p] / page_size] * page_size + positions[p] % page_size.
- *     Tokens the device checks would skip take no part.  The check is for
- *     debugging: it synchronises, so it does not belong in a captured graph.
+ *     pkv_decode, pkv_decode_static, pkv_step and pkv_prefill first
+ *     synchronise the stream, copy the call's positions, rows, slots and table
+ *     to the host and return PKV_EINVAL (nothing enqueued) when two written
+ *     slots coincide outside pool page 0, when a given prompt slot differs from
+ *     table[rows[p]][positions[p] / page_size] * page_size + positions[p] % page_size,
+ *     or, for the decode entries, when a row reads (at a position up to its
+ *     own) a slot that another row of the call writes -- the one ordering
+ *     decode does not provide (see pkv_decode).  Tokens the device checks
+ *     would skip take no part.  The check is for debugging: it synchronises,
+ *     so it does not belong in a captured graph.
  *   - Calls on one pool may run concurrently on different streams as long as
  *     they write different slots.  Each pkv_decode / pkv_step call takes one
  *     of the pool's 32 work counters in turn (zero between calls), so at most
@@ -294,6 +297,41 @@ PKV_API int pkv_linear(pkv_pool* pool, const void* x, const void* w, void* y, in
 PKV_API int pkv_qkv_proj(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden, void* q, void* k,
                          void* v, void* stream);
 
+/* ---- the projection with the per-token work fused in, and the attention after it --------
+ * qwen3-8b Nest files, src/attention.linnet, GroupedQueryAttention.decode_paged:
+ *   q = rope_rows(q_norm(split_heads(q_proj(x))))
+ *   k = rope_rows(k_norm(split_heads(k_proj(x)))),  v = split_heads(v_proj(x))
+ *   write_tokens(k, v at page_slots(table, positions))
+ * in one launch, for `tokens` decode rows (token t is table row t, at
+ * positions[t]): the product of pkv_qkv_proj, whose epilogue -- each 128-feature
+ * tile of the product is one head, all of it in the CTA that finishes it --
+ * rounds q, k, v to bf16 (the pages' projection outputs), applies QK-norm and
+ * RoPE to q and k exactly as pkv_decode does, writes k and v to their slots of
+ * the pool and q to q_hat.  The raw q, k, v never reach memory.
+ *   x, w_qkv   as pkv_qkv_proj (hidden % 64 == 0, PKV_ENOTIMPL otherwise)
+ *   q_norm_w, k_norm_w  device bf16 [head_dim]
+ *   positions  device int32 [tokens]; -1 = no step (nothing written)
+ *   table      device int32 [tokens][pages], or NULL (contiguous rows)
+ *   q_hat      device fp32 [tokens][heads][head_dim], 16-byte aligned (out):
+ *              QK-normed, roped q, unscaled
+ * Rows whose position or pages pkv_decode would reject are not written and set
+ * the same device error bits.  Slots must be distinct (PKV_CHECK=1 checks).
+ * Follow it with pkv_decode_appended on the same stream. */
+PKV_API int pkv_qkv_proj_append(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden,
+                                const void* q_norm_w, const void* k_norm_w, const int32_t* positions,
+                                const int32_t* table, int pages, float* q_hat, void* stream);
+
+/* decode_paged's attention for rows whose q was prepared and whose k and v
+ * were appended by pkv_qkv_proj_append (the same positions and table): row b
+ * attends over positions 0..positions[b] of table[b], with q_hat[b] (fp32
+ * [rows][heads][head_dim]).  Nothing is written to the pool, so rows may
+ * read each other's new slots (the call that wrote them has completed before
+ * this one on the stream).  Workspace, output, skipped rows and error bits as
+ * pkv_decode. */
+PKV_API int pkv_decode_appended(pkv_pool* pool, const float* q_hat, const int32_t* positions, const int32_t* table,
+                                int rows, int pages, void* out, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
 /* ---- output gate of the gated-attention variant ----------------------------------------
  * fantasma model.zig, fullAttentionForward ("Full Attention (GQA with output gate +
  * QK-norm + partial RoPE)"): the q projection also yields a gate per head and
@@ -317,11 +355,15 @@ PKV_API int pkv_output_gate(pkv_pool* pool, void* out, const void* gate, int tok
  * Instead of a caller workspace it uses a scratch array compiled into the
  * library: PKV_STATIC_SCRATCH_BYTES (32 MiB) of device memory that every GPU
  * that loads the library holds until the process exits.  The call itself
- * allocates nothing.  The caller still passes the pool, inputs and output,
- * exactly as for pkv_decode (same layouts, same error codes), minus the
- * workspace.
- *   - The first call on each device looks up the array's device address, with
- *     that device current.  Make that first call before any stream capture.
+ * allocates no device memory.  The caller still passes the pool, inputs and
+ * output, exactly as for pkv_decode (same layouts, same error codes, the same
+ * PKV_CHECK=1 debugging pre-check, which copies the call's tables into host
+ * memory), minus the workspace.
+ *   - Each call whose stream is not being captured looks up the array's
+ *     device address on the current device (so the array reloaded after a
+ *     cudaDeviceReset is found again); a call under stream capture reuses the
+ *     address the last uncaptured call on that device found.  Make one call
+ *     on each device before capturing any.
  *   - Every call shares the one array, which keeps the last call's contents.
  *     Nothing in it needs to start at zero.  Calls whose work overlaps on the
  *     GPU (e.g. on two streams with no ordering between them) race on the array
@@ -350,13 +392,27 @@ PKV_API int pkv_check_errors(pkv_pool* pool, void* stream, uint32_t* flags);
  * pkv_workspace_bytes.  Errors: PKV_EINVAL (null, < 0). */
 PKV_API int pkv_set_ctas(pkv_pool* pool, int ctas);
 
+/* Limit, in nanoseconds, of each bounded wait inside the decode attention
+ * kernel (the shared-memory ring between its copy warp and its compute warps,
+ * and the compute warps' meeting points); default 1e9 (one second).  A wait
+ * that runs out makes its CTA stop: it sets PKV_DEVERR_TIMEOUT in the error
+ * word, lets the copies it has in flight land (allowing a full second for
+ * that, whatever this limit), and exits; the outputs of that call are void,
+ * and the pool is ready for the next call.  0 gives up at the first check
+ * that finds the awaited data not yet there, which lets a test run the
+ * timeout path on purpose.  Applies to calls enqueued after it.
+ * Errors: PKV_EINVAL (null, ns < 0). */
+PKV_API int pkv_set_wait_limit(pkv_pool* pool, int64_t ns);
+
 /* Kernel timer: while enabled, every pkv_decode / pkv_step records a pair of
  * CUDA events on its stream around the decode attention kernel (the dominant
  * launch), every pkv_prefill around its prompt-attention kernel and every
  * pkv_linear around its matrix-product kernel.  pkv_timer_read synchronises on the last recorded event,
  * returns the summed duration in milliseconds and the number of timed
  * launches since the timer was last enabled, and keeps the timer running.
- * At most 4096 launches are kept (later ones overwrite the oldest). */
+ * At most 4096 launches are kept (later ones overwrite the oldest).  Host
+ * threads sharing a pool take distinct event slots; pkv_timer_enable and
+ * pkv_timer_read should not race with calls in flight on other threads. */
 PKV_API int pkv_timer_enable(pkv_pool* pool, int enable);
 PKV_API int pkv_timer_read(pkv_pool* pool, double* total_ms, int64_t* launches);
 

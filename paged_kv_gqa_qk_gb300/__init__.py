@@ -26,8 +26,9 @@ PKV_DEVERR_POSITION, PKV_DEVERR_PAGE, PKV_DEVERR_ROW, PKV_DEVERR_SLOT, PKV_DEVER
 # Every symbol include/pkv.h declares.
 ABI_SYMBOLS = ("pkv_config_default", "pkv_strerror", "pkv_pool_alloc", "pkv_pool_wrap", "pkv_pool_free",
                "pkv_pool_kv", "pkv_workspace_bytes", "pkv_decode", "pkv_step", "pkv_prefill", "pkv_check_errors",
-               "pkv_set_ctas", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static",
-               "pkv_linear_workspace_bytes", "pkv_linear", "pkv_qkv_proj", "pkv_output_gate")
+               "pkv_set_ctas", "pkv_set_wait_limit", "pkv_timer_enable", "pkv_timer_read", "pkv_decode_static",
+               "pkv_linear_workspace_bytes", "pkv_linear", "pkv_qkv_proj", "pkv_qkv_proj_append",
+               "pkv_decode_appended", "pkv_output_gate")
 
 # Size of the scratch array pkv_decode_static uses in place of a workspace.
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
@@ -75,12 +76,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "pkv_prefill": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, sz, vp], i32),
         "pkv_check_errors": ([vp, vp, ctypes.POINTER(ctypes.c_uint32)], i32),
         "pkv_set_ctas": ([vp, i32], i32),
+        "pkv_set_wait_limit": ([vp, i64], i32),
         "pkv_timer_enable": ([vp, i32], i32),
         "pkv_timer_read": ([vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)], i32),
         "pkv_decode_static": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp], i32),
         "pkv_linear_workspace_bytes": ([vp, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "pkv_linear": ([vp, vp, vp, vp, i32, i32, i32, vp, sz, vp], i32),
         "pkv_qkv_proj": ([vp, vp, vp, i32, i32, vp, vp, vp, vp], i32),
+        "pkv_qkv_proj_append": ([vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, vp, vp], i32),
+        "pkv_decode_appended": ([vp, vp, vp, vp, i32, i32, vp, vp, sz, vp], i32),
         "pkv_output_gate": ([vp, vp, vp, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
@@ -268,6 +272,30 @@ def pkv_qkv_proj(pool, x, w_qkv, q, k, v, stream=None) -> None:
         "pkv_qkv_proj")
 
 
+def pkv_qkv_proj_append(pool, x, w_qkv, q_norm_w, k_norm_w, positions, table, q_hat, stream=None,
+                        pages=None) -> None:
+    """q/k/v projection of decode rows with QK-norm, RoPE and the k/v append in its epilogue;
+    q_hat (fp32 [tokens][heads][head_dim]) receives the normed, roped q."""
+    tokens, hidden = int(x.shape[0]), int(x.shape[1])
+    tp, rows, pages = _table(table, positions.shape[0], pages)
+    if rows != tokens or q_hat.shape[0] != tokens:
+        raise ValueError(f"x has {tokens} tokens, positions/table {rows}, q_hat {q_hat.shape[0]}")
+    _check(load_library().pkv_qkv_proj_append(
+        pool, _dev(x, torch.bfloat16, "x"), _dev(w_qkv, torch.bfloat16, "w_qkv"), tokens, hidden,
+        _dev(q_norm_w, torch.bfloat16, "q_norm_w"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
+        _dev(positions, torch.int32, "positions"), tp, pages, _dev(q_hat, torch.float32, "q_hat"),
+        _stream(stream)), "pkv_qkv_proj_append")
+
+
+def pkv_decode_appended(pool, q_hat, positions, table, out, workspace, stream=None, pages=None) -> None:
+    """decode_paged's attention after pkv_qkv_proj_append (q prepared, k/v already in the pool)."""
+    tp, rows, pages = _table(table, positions.shape[0], pages)
+    _check(load_library().pkv_decode_appended(
+        pool, _dev(q_hat, torch.float32, "q_hat"), _dev(positions, torch.int32, "positions"), tp, rows, pages,
+        _dev(out, torch.bfloat16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)), "pkv_decode_appended")
+
+
 def pkv_output_gate(pool, out, gate, stream=None) -> None:
     """out *= sigmoid(gate) in place (the gated-attention variant's output gate)."""
     if out.shape != gate.shape:
@@ -284,6 +312,10 @@ def pkv_check_errors(pool, stream=None) -> int:
 
 def pkv_set_ctas(pool, ctas: int) -> None:
     _check(load_library().pkv_set_ctas(pool, int(ctas)), "pkv_set_ctas")
+
+
+def pkv_set_wait_limit(pool, ns: int) -> None:
+    _check(load_library().pkv_set_wait_limit(pool, int(ns)), "pkv_set_wait_limit")
 
 
 def pkv_timer_enable(pool, enable: bool) -> None:
@@ -371,6 +403,20 @@ class PagedKVPool:
             v = torch.empty(n, c.kv_heads, c.head_dim, dtype=torch.bfloat16, device=x.device)
         pkv_qkv_proj(self.handle, x, w_qkv, q, k, v, stream)
         return q, k, v
+
+    def decode_layer_fused(self, x, w_qkv, q_norm_w, k_norm_w, positions, table, out=None, q_hat=None,
+                           stream=None, pages=None) -> torch.Tensor:
+        """The q/k/v projection with norm, RoPE and append fused in, then the attention."""
+        c, n = self.cfg, x.shape[0]
+        if q_hat is None:
+            q_hat = torch.empty(n, c.heads, c.head_dim, dtype=torch.float32, device=x.device)
+        if out is None:
+            out = torch.empty(n, c.heads, c.head_dim, dtype=torch.bfloat16, device=x.device)
+        pages = table.shape[1] if table is not None else pages
+        pkv_qkv_proj_append(self.handle, x, w_qkv, q_norm_w, k_norm_w, positions, table, q_hat, stream, pages=pages)
+        ws = self.workspace(n, pages, 0)
+        pkv_decode_appended(self.handle, q_hat, positions, table, out, ws, stream, pages=pages)
+        return out
 
     def check_errors(self, stream=None) -> int:
         return pkv_check_errors(self.handle, stream)

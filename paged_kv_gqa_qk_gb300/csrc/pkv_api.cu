@@ -9,6 +9,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <array>
+#include <climits>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -67,15 +69,12 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
 {
     const bool decode = a.P == 0;
     const bool timed = pool->timer_on;
-    const int slot = (int)(pool->timer_count % kTimerSlots);
+    const int slot = timed ? (int)(pool->timer_count.fetch_add(1) % kTimerSlots) : 0;
     if (!decode && a.steps == 0) {  // prompts only: prep -> prompt-token attention (the timed kernel)
         if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
         if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
-        if (launch_prefill(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
-        if (timed) {
-            if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
-            pool->timer_count++;
-        }
+        if (launch_prefill(pool, a, plan, pool->num_sms, s) != cudaSuccess) return PKV_ECUDA;
+        if (timed && cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
         return PKV_OK;
     }
     StepArgs as = a;  // the tokens the attention + combine kernels see
@@ -83,7 +82,7 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
     ps.claim = pool->claims + (pool->call_seq++ % kClaimSlots);
     if (!decode) {
         if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
-        if (launch_prefill(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
+        if (launch_prefill(pool, a, plan, pool->num_sms, s) != cudaSuccess) return PKV_ECUDA;
         // the step rows are tokens P..P+rows-1
         const size_t qrow = (size_t)pool->cfg.heads * pool->cfg.head_dim * 2;
         as.q = static_cast<const char*>(a.q) + (size_t)a.P * qrow;
@@ -94,10 +93,7 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
     }
     if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
     if (launch_attn(pool, as, ps, decode, !timed, s) != cudaSuccess) return PKV_ECUDA;
-    if (timed) {
-        if (cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
-        pool->timer_count++;
-    }
+    if (timed && cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
     if (launch_combine(pool, as, ps, decode, s) != cudaSuccess) {
         // the combine resets this call's chunk counter; without it, reset it here
         cudaMemsetAsync(ps.claim, 0, sizeof(uint32_t), s);
@@ -220,6 +216,7 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
     p->num_pages = num_pages;
     p->num_slots = num_slots;
     p->owns_kv = owns;
+    p->wait_ns = 1000000000ull;
     const size_t kv_bytes = (size_t)cfg->kv_heads * num_slots * cfg->head_dim * 2;
     const size_t tab = (size_t)cfg->max_seq * (cfg->head_dim / 2) * sizeof(float2);
     bool fail = false;
@@ -269,7 +266,7 @@ static int create_pool(const pkv_config* cfg, int num_pages, void* k, void* v, b
 static bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // ---- optional host pre-check (environment variable PKV_CHECK=1) ----------------------------
-static bool check_enabled()
+bool check_enabled()
 {
     const char* e = std::getenv("PKV_CHECK");
     return e && e[0] == '1' && e[1] == 0;
@@ -277,10 +274,12 @@ static bool check_enabled()
 
 // Copies the call's token tables to the host (synchronising the stream first)
 // and rejects, with PKV_EINVAL, a call whose written slots are not distinct
-// outside pool page 0 or whose given prompt slots differ from those the table
-// derives.  Tokens the device would skip (position, row or page out of range)
-// take no part: the device checks report them.
-static int host_precheck(const pkv_pool* pool, const StepArgs& a, cudaStream_t s)
+// outside pool page 0, whose given prompt slots differ from those the table
+// derives, or -- decode only, where each row's write is ordered before its own
+// reads but not before other rows' -- in which a row reads a slot another row
+// of the call writes.  Tokens the device would skip (position, row or page out
+// of range) take no part: the device checks report them.
+int host_precheck(const pkv_pool* pool, const StepArgs& a, cudaStream_t s)
 {
     if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ECUDA;
     auto fetch = [](const int32_t* src, size_t n, std::vector<int32_t>& dst) {
@@ -323,6 +322,28 @@ static int host_precheck(const pkv_pool* pool, const StepArgs& a, cudaStream_t s
     std::sort(written.begin(), written.end());
     for (size_t i = 1; i < written.size(); ++i)
         if (written[i] == written[i - 1] && written[i] >= S) return PKV_EINVAL;
+    if (a.P == 0 && a.steps > 0 && !a.q_hat) {
+        // decode: no row may read (position s <= its own) a slot another row writes.
+        // (page id, row, offset in page) of every write, sorted by page id
+        std::vector<std::array<int64_t, 3>> w;
+        for (int b = 0; b < a.steps; ++b) {
+            if (steps[b] == -1) continue;
+            const int64_t d = derive(b, steps[b]);
+            if (d >= 0) w.push_back({d / S, b, d % S});
+        }
+        std::sort(w.begin(), w.end());
+        for (int b = 0; b < a.steps; ++b) {
+            if (steps[b] == -1 || derive(b, steps[b]) < 0) continue;
+            const int last = steps[b] / S;
+            for (int j = 0; j <= last; ++j) {
+                const int64_t id = page(b, j);
+                const int64_t lim = j == last ? steps[b] % S : S - 1;  // offsets row b reads in this page
+                auto it = std::lower_bound(w.begin(), w.end(), std::array<int64_t, 3>{id, INT64_MIN, INT64_MIN});
+                for (; it != w.end() && (*it)[0] == id; ++it)
+                    if ((*it)[1] != b && (*it)[2] <= lim) return PKV_EINVAL;
+            }
+        }
+    }
     return PKV_OK;
 }
 
@@ -436,6 +457,7 @@ int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, cons
                const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows, int pages,
                void* out, void* workspace, size_t workspace_bytes, void* stream)
 {
+    NvtxRange range("pkv_decode");
     if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !out) return PKV_EINVAL;
     if (rows <= 0 || pages <= 0) return PKV_EINVAL;
     if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
@@ -448,11 +470,57 @@ int pkv_decode(pkv_pool* pool, const void* q, const void* k, const void* v, cons
     return run_step(pool, a, workspace_bytes, stream);
 }
 
+int pkv_qkv_proj_append(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden,
+                        const void* q_norm_w, const void* k_norm_w, const int32_t* positions, const int32_t* table,
+                        int pages, float* q_hat, void* stream)
+{
+    NvtxRange range("pkv_qkv_proj_append");
+    if (!pool || !x || !w_qkv || !q_norm_w || !k_norm_w || !positions || !q_hat) return PKV_EINVAL;
+    if (tokens <= 0 || hidden <= 0 || pages <= 0) return PKV_EINVAL;
+    if (hidden % 64) return PKV_ENOTIMPL;
+    if (tokens > (1 << 20) || hidden > (1 << 20) || (int64_t)tokens * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(x, 16) || !aligned(w_qkv, 16) || !aligned(q_hat, 16) || !aligned(q_norm_w, 8) ||
+        !aligned(k_norm_w, 8) || !aligned(positions, 4) || !aligned(table, 4))
+        return PKV_EINVAL;
+    if (!table && (int64_t)tokens * pages > pool->num_pages) return PKV_ERANGE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (check_enabled()) {  // written slots must be distinct (the append is a scatter)
+        const StepArgs a = {nullptr, nullptr, nullptr, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions,
+                            table, 0, tokens, pages, tokens, nullptr, nullptr, q_hat};
+        const int rc = host_precheck(pool, a, s);
+        if (rc != PKV_OK) return rc;
+    }
+    const QkvAppend fa = {q_norm_w, k_norm_w, positions, table, pages, q_hat};
+    return launch_qkv_append(pool, x, w_qkv, tokens, hidden, fa, s) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int pkv_decode_appended(pkv_pool* pool, const float* q_hat, const int32_t* positions, const int32_t* table, int rows,
+                        int pages, void* out, void* workspace, size_t workspace_bytes, void* stream)
+{
+    NvtxRange range("pkv_decode_appended");
+    if (!pool || !q_hat || !positions || !out) return PKV_EINVAL;
+    if (rows <= 0 || pages <= 0) return PKV_EINVAL;
+    if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
+    if (!aligned(q_hat, 16) || !aligned(out, 8) || !aligned(positions, 4) || !aligned(table, 4)) return PKV_EINVAL;
+    if (workspace && !aligned(workspace, 256)) return PKV_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
+    if (!table && (int64_t)rows * pages > pool->num_pages) return PKV_ERANGE;
+    const Plan plan = make_plan(pool, rows, pages);
+    if (!workspace || workspace_bytes < plan.total) return PKV_EWORKSPACE;
+    const StepArgs a = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, positions, table,
+                        0, rows, pages, rows, out, static_cast<char*>(workspace), q_hat};
+    return enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
+}
+
 int pkv_step(pkv_pool* pool, const void* q, const void* k, const void* v, const void* q_norm_w,
              const void* k_norm_w, const int32_t* positions, const int32_t* prow, const int32_t* slots,
              const int32_t* step_positions, const int32_t* table, int P, int rows, int pages, void* out,
              void* workspace, size_t workspace_bytes, void* stream)
 {
+    NvtxRange range("pkv_step");
     if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !prow || !step_positions || !out)
         return PKV_EINVAL;
     if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
@@ -472,6 +540,7 @@ int pkv_prefill(pkv_pool* pool, const void* q, const void* k, const void* v, con
                 const int32_t* table, int P, int rows, int pages, void* out, void* workspace,
                 size_t workspace_bytes, void* stream)
 {
+    NvtxRange range("pkv_prefill");
     if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !prow || !out) return PKV_EINVAL;
     if (P <= 0 || rows <= 0 || pages <= 0) return PKV_EINVAL;
     if (P > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
@@ -564,6 +633,13 @@ int pkv_set_ctas(pkv_pool* pool, int ctas)
     return PKV_OK;
 }
 
+int pkv_set_wait_limit(pkv_pool* pool, int64_t ns)
+{
+    if (!pool || ns < 0) return PKV_EINVAL;
+    pool->wait_ns = (uint64_t)ns;
+    return PKV_OK;
+}
+
 int pkv_timer_enable(pkv_pool* pool, int enable)
 {
     if (!pool) return PKV_EINVAL;
@@ -587,13 +663,14 @@ int pkv_timer_read(pkv_pool* pool, double* total_ms, int64_t* launches)
     if (!pool || !total_ms || !launches) return PKV_EINVAL;
     *total_ms = 0.0;
     *launches = 0;
-    if (!pool->ev_start || pool->timer_count == 0) return PKV_OK;
-    const int64_t n = pool->timer_count < kTimerSlots ? pool->timer_count : kTimerSlots;
-    const int last = (int)((pool->timer_count - 1) % kTimerSlots);
+    const int64_t cnt = pool->timer_count.load();
+    if (!pool->ev_start || cnt == 0) return PKV_OK;
+    const int64_t n = cnt < kTimerSlots ? cnt : kTimerSlots;
+    const int last = (int)((cnt - 1) % kTimerSlots);
     if (cudaEventSynchronize(pool->ev_stop[last]) != cudaSuccess) return PKV_ECUDA;
     double sum = 0.0;
     for (int64_t i = 0; i < n; ++i) {
-        const int sl = (int)((pool->timer_count - 1 - i) % kTimerSlots);
+        const int sl = (int)((cnt - 1 - i) % kTimerSlots);
         float ms = 0.f;
         if (cudaEventElapsedTime(&ms, pool->ev_start[sl], pool->ev_stop[sl]) != cudaSuccess) return PKV_ECUDA;
         sum += ms;

@@ -9,6 +9,8 @@
 
 #include <atomic>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pkv.h"
 
 namespace pkv {
@@ -48,9 +50,11 @@ struct pkv_pool {
     CUtensorMap tmap_v;
     int ctas_per_sm;       // resident attention CTAs per SM (occupancy)
     int ctas_override;     // attention grid size; 0 = one wave (ctas_per_sm x SMs)
-    // kernel timer
+    uint64_t wait_ns;      // limit of the decode attention kernel's ring and group waits (default 1 s)
+    // kernel timer: a timed call takes event slot timer_count++ % kTimerSlots (atomic,
+    // so host threads sharing the pool take distinct slots)
     bool timer_on;
-    int64_t timer_count;
+    std::atomic<int64_t> timer_count;
     cudaEvent_t* ev_start;
     cudaEvent_t* ev_stop;
 };
@@ -88,6 +92,16 @@ struct StepArgs {
     int steps;                      // step tokens (rows for decode and step, 0 for prefill)
     void* out;
     char* ws;
+    const float* q_hat;             // decode with q prepared and k/v appended beforehand, or null
+};
+
+// An NVTX range over one entry-point call (its host-side enqueue), for
+// timeline tools; a no-op unless a tool is attached.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 // Pool page holding page j of table row `row` (a null table: contiguous rows).
@@ -108,6 +122,19 @@ int linear_splits(const pkv_pool* pool, int tokens, int in, int out);
 cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, int tokens, int in, int nseg,
                           void* const* y, const int* widths, cudaStream_t s);
 
+// pkv_qkv_proj_append: the q/k/v projection of `tokens` decode rows (token t =
+// table row t) with QK-norm, RoPE and the k/v append done by its epilogue.
+struct QkvAppend {
+    const void* q_norm_w;
+    const void* k_norm_w;
+    const int32_t* positions;  // [tokens]
+    const int32_t* table;      // [tokens][pages], or null (contiguous rows)
+    int pages;
+    float* q_hat;              // [tokens][heads][head_dim] fp32 out
+};
+cudaError_t launch_qkv_append(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden,
+                              const QkvAppend& a, cudaStream_t s);
+
 // out *= sigmoid(gate) over n bf16 elements (n % 8 == 0, 16-byte aligned).
 cudaError_t launch_gate(const pkv_pool* pool, void* out, const void* gate, int64_t n, cudaStream_t s);
 
@@ -126,10 +153,18 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
                         cudaStream_t s);
 cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& plan, bool decode_mode,
                            cudaStream_t s);
-// step mode: prompt-token attention on tcgen05 tensor cores (pkv_prefill.cu)
-cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
+// step mode: prompt-token attention on tcgen05 tensor cores (pkv_prefill.cu), a
+// persistent grid of `ctas` CTAs (one per SM; capped at its work units)
+cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, cudaStream_t s);
 
 // Enqueue one decode (a.P == 0) or step call on workspace a.ws; host checks done.
 int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);
+
+// The optional host pre-check (environment variable PKV_CHECK=1): synchronises
+// s, copies the call's token tables to the host and returns PKV_EINVAL for a
+// call whose written slots coincide outside page 0, whose given prompt slots
+// disagree with the table, or (decode) whose rows read another row's new slot.
+bool check_enabled();
+int host_precheck(const pkv_pool* pool, const StepArgs& a, cudaStream_t s);
 
 }  // namespace pkv

@@ -26,109 +26,9 @@
 
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
+#include "pkv_rope.cuh"
 
 namespace pkv {
-
-constexpr uint32_t kFull = 0xffffffffu;
-
-__device__ __forceinline__ void unpack4(uint2 r, float (&x)[4])
-{
-    x[0] = __uint_as_float(r.x << 16);
-    x[1] = __uint_as_float(r.x & 0xffff0000u);
-    x[2] = __uint_as_float(r.y << 16);
-    x[3] = __uint_as_float(r.y & 0xffff0000u);
-}
-
-__device__ __forceinline__ uint2 pack4(const float (&y)[4])
-{
-    uint2 r;
-    r.x = pack_bf16(__float2bfloat16_rn(y[0]), __float2bfloat16_rn(y[1]));
-    r.y = pack_bf16(__float2bfloat16_rn(y[2]), __float2bfloat16_rn(y[3]));
-    return r;
-}
-
-// k after QK-norm + rotate-half RoPE, for the warp that holds one k head
-// (lane l: elements 4l..4l+3; the rotate-half partner of element i < 64 is
-// i + 64, in lane l ^ 16):
-//   RMSNorm: x / sqrt(mean(x^2) + eps) * w;  RoPE: y*cos + rotate_half(y)*sin.
-// Both are linear in y, so the normaliser goes last:
-//   r = inv * a,  a = u*cos -/+ u'*sin,  u = x*w (exact in fp32: bf16 x bf16).
-// k is stored in bf16, and when the two terms of a cancel, plain fp32 loses
-// far more than a bf16 ulp.  So a is formed without error growth: cos and sin
-// come as fp32 hi + lo pairs of the double values, the products' rounding
-// errors are recovered exactly with fma and the sum's with two-sum; the
-// result has fp32 accuracy relative to a itself, and rounds to within one
-// bf16 ulp of the exact value.
-__device__ __forceinline__ float rotate_exact(float u, float up, float2 hi, float2 lo)
-{
-    const float p1 = __fmul_rn(u, hi.x), e1 = __fmaf_rn(u, hi.x, -p1);
-    const float p2 = __fmul_rn(up, hi.y), e2 = __fmaf_rn(up, hi.y, -p2);
-    const float s = __fadd_rn(p1, p2);
-    const float bp = __fsub_rn(s, p1);
-    const float e3 = __fadd_rn(__fsub_rn(p1, __fsub_rn(s, bp)), __fsub_rn(p2, bp));
-    const float lo_terms = __fmaf_rn(u, lo.x, __fmaf_rn(up, lo.y, __fadd_rn(__fadd_rn(e1, e2), e3)));
-    return __fadd_rn(s, lo_terms);
-}
-
-// RoPE layout of a warp holding one head, 4 consecutive dims per lane: with R
-// rotated dims, lanes below R/8 hold the first rotary half (partner: R/2
-// dims, i.e. R/8 lanes, up), lanes in [R/8, R/4) the second (partner R/8 lanes
-// down), and lanes from R/4 up the dims RoPE leaves as they are.
-struct KRope {
-    int src;     // lane holding this lane's partner dims
-    float sgn;   // -1: first half (u cos - partner sin), +1: second (u cos + partner sin)
-    int f0;      // table index of this lane's first dim
-    bool rot;    // false: not rotated
-};
-__device__ __forceinline__ KRope krope(int lane, int rot)
-{
-    const int hl = rot / 8;
-    KRope r;
-    r.rot = lane < 2 * hl;
-    const bool first = lane < hl;
-    r.src = first ? lane + hl : (r.rot ? lane - hl : lane);
-    r.sgn = first ? -1.f : 1.f;
-    r.f0 = r.rot ? 4 * (first ? lane : lane - hl) : 0;
-    return r;
-}
-
-// The warp's normed + roped k as 4 bf16 (this lane's elements).
-//   kraw: this lane's 4 raw bf16;  wk: its k_norm weights;
-//   rh/rl: (cos, sin) hi and lo parts at the token's position for this lane's
-//   table entries krope(lane, rot).f0 .. + 3;  rot: the rotated dims.
-__device__ __forceinline__ uint2 norm_rope_k_regs(uint2 kraw, const float (&wk)[4], const float2 (&rh)[4],
-                                                  const float2 (&rl)[4], float eps, int lane, int rot)
-{
-    float x[4];
-    unpack4(kraw, x);
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-    const float inv = rsqrtf(ss * (1.0f / kHeadDim) + eps);
-    const KRope kr = krope(lane, rot);
-    __nv_bfloat16 r[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float u = x[i] * wk[i];
-        const float partner = kr.sgn * __shfl_sync(kFull, u, kr.src);
-        r[i] = __float2bfloat16_rn(__fmul_rn(kr.rot ? rotate_exact(u, partner, rh[i], rl[i]) : u, inv));
-    }
-    return make_uint2(pack_bf16(r[0], r[1]), pack_bf16(r[2], r[3]));
-}
-
-//   rhi/rlo: (cos, sin) hi and lo parts of the token's position, [64].
-__device__ __forceinline__ uint2 norm_rope_k(uint2 kraw, const float (&wk)[4], const float2* rhi, const float2* rlo,
-                                             float eps, int lane, int rot)
-{
-    const KRope kr = krope(lane, rot);
-    float2 rh[4], rl[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        rh[i] = rhi[kr.f0 + i];
-        rl[i] = rlo[kr.f0 + i];
-    }
-    return norm_rope_k_regs(kraw, wk, rh, rl, eps, lane, rot);
-}
 
 // =====================================================================================
 // prep_kernel (step mode): validate every token, append every token's k and v
@@ -363,8 +263,28 @@ __device__ __forceinline__ void q_prep(const uint32_t (&xr)[8][2], const uint32_
     }
 }
 
+// B fragments of q for one head, from q already normed and roped (fp32, the
+// head's 128 dims at qf; pkv_qkv_proj_append's output): the dims
+// 16 ks + 2 tig + {0, 1, 8, 9} of this lane, times the score scale, split into
+// a bf16 head (prt 0) or the bf16 of its remainder (prt 1).
+__device__ __forceinline__ void q_from_hat(const float* qf, float scale, int tig, int prt, uint32_t (&bq)[8][2])
+{
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const float2 lo = *reinterpret_cast<const float2*>(qf + 16 * ks + 2 * tig);
+        const float2 hi = *reinterpret_cast<const float2*>(qf + 16 * ks + 2 * tig + 8);
+        const float y[4] = {lo.x * scale, lo.y * scale, hi.x * scale, hi.y * scale};
+        __nv_bfloat16 h[4], t[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) split_bf16(y[k], h[k], t[k]);
+        bq[ks][0] = prt ? pack_bf16(t[0], t[1]) : pack_bf16(h[0], h[1]);
+        bq[ks][1] = prt ? pack_bf16(t[2], t[3]) : pack_bf16(h[2], h[3]);
+    }
+}
+
 struct AttnParams {
     const __nv_bfloat16* q;   // [ntok][heads][128] projected q (normed + roped here)
+    const float* qhat;        // prepared mode: [ntok][heads][128] q already normed + roped, fp32
     const __nv_bfloat16* k;   // [ntok][kv_heads][128]  (decode mode: appended here)
     const __nv_bfloat16* v;
     const __nv_bfloat16* qw;
@@ -385,8 +305,11 @@ struct AttnParams {
     int32_t* unit_ok;         // [U], written by the CTA holding each unit's first page
     uint32_t* err;
     int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode, rot;
+    int rows;                 // table rows (for the neighbouring-row comparison of shared pages)
+    int prepared;             // decode mode with q prepared and k/v appended beforehand (pkv_decode_appended)
     int64_t num_slots;
     float eps;
+    uint64_t wait_ns;         // limit of the ring and group waits (the final drain always allows kWaitLimitNs)
 };
 
 constexpr int kConsumerWarps = 4;
@@ -413,7 +336,7 @@ struct AttnSmem {
     static constexpr int kSum = kScan + 32;                   // int [threads] first token, int [threads] prefix
     static constexpr int kW = kSum + 2 * kAttnThreads * 4;    // bf16 q_norm_w [128], k_norm_w [128]
     static constexpr int kBars = kW + 512;                    // u64 full[S], empty[S], group
-    static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);
+    static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);  // int abort, items issued, stop item sent
     static constexpr int kBytes = kFlag + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
 };
@@ -490,12 +413,13 @@ __device__ __forceinline__ void token_info(const AttnParams& p, int t, int& row,
     }
 }
 
-// The four consumer warps meet at an mbarrier (bounded wait, unlike bar.sync).
-__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int lane)
+// The four consumer warps meet at an mbarrier (bounded wait, unlike bar.sync);
+// the result is the same on every lane of the warp.
+__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, int lane, uint64_t limit_ns)
 {
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait_spin(bar, phase & 1);
+    const bool ok = __all_sync(kFull, mbar_wait_spin(bar, phase & 1, limit_ns));
     ++phase;
     return ok;
 }
@@ -559,6 +483,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const uint32_t bar_empty = bar_full + 8 * kStages;
     const uint32_t bar_group = bar_empty + 8 * kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kFlag);
+    volatile int* s_issued = abort_flag + 1;     // ring items the producer loaded (copies in flight at most kStages)
+    volatile int* s_stop_sent = abort_flag + 2;  // the producer's final item (no data) went out
     float* sM = reinterpret_cast<float*>(sbase + L::kM);
     float* sL = reinterpret_cast<float*>(sbase + L::kL);
     int4* sMeta = reinterpret_cast<int4*>(sbase + L::kMeta);
@@ -578,6 +504,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
         mbar_init(bar_group, kConsumerWarps);
         *abort_flag = 0;
+        *s_issued = 0;
+        *s_stop_sent = 0;
         fence_mbar_init();
     }
     if (warp == kProducerWarp && lane == 0) {
@@ -594,8 +522,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
     // the norm weights, read once here (under the kernel's own streaming a
     // global load can wait microseconds)
-    if (tid < 32) sW[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
-    else if (tid < 64) sW[tid] = reinterpret_cast<const uint2*>(p.kw)[tid - 32];
+    if (!p.prepared) {
+        if (tid < 32) sW[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
+        else if (tid < 64) sW[tid] = reinterpret_cast<const uint2*>(p.kw)[tid - 32];
+    }
 
     // ---- pages per token and their exclusive prefix over tokens (every CTA computes it)
     const int nt = p.ntok;
@@ -638,7 +568,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         // ================================================================ producer
         int i = 0;  // ring items issued
         bool ok = true;
-        const uint64_t pol = l2_policy_evict_first();
+        // Pages are read once, except the pages several rows share (a shared prompt
+        // prefix): those stay in L2 for the other rows' reads, the rest go first.
+        const uint64_t pol = l2_policy_evict_first(), pol_shared = l2_policy_evict_last();
         // the static slice, then one claimed chunk after another; each claim is
         // made when the range before it starts, so its answer is there at the end
         int64_t xb = (int64_t)c * sp.S / sp.Ce, xe = (int64_t)(c + 1) * sp.S / sp.Ce;
@@ -673,17 +605,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                     if (!valid && g == 0) atomicOr(p.err, PKV_DEVERR_PAGE);
                 }
                 const bool has_last = j + seg == n;
-                const bool append = p.decode_mode && valid && has_last;
+                const bool append = p.decode_mode && !p.prepared && valid && has_last;
                 const int seg_flags = (valid ? kFlagValid : 0) | ((j == 0 && has_last) ? kFlagComplete : 0);
                 for (int s = 0; s < seg; ++s, ++i) {
                     const int jj = j + s, st = i % kStages;
-                    if (i >= kStages && (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag)) {
+                    if (i >= kStages &&
+                        __any_sync(kFull, !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1, p.wait_ns) ||
+                                              *abort_flag)) {
                         ok = false;
                         break;
                     }
-                    int page = 0;
-                    if (lane == 0 && valid) page = page_of(p.table, p.pages, row, jj);
-                    page = __shfl_sync(kFull, page, 0);
+                    // lane 0: the page; lanes 1 and 2: the same column of the rows before and
+                    // after, so that a prefix page shared with a neighbouring row is known
+                    int pg = -1;
+                    if (valid && lane < 3) {
+                        const int r2 = row + (lane == 0 ? 0 : (lane == 1 ? -1 : 1));
+                        if (lane == 0 || (p.table && r2 >= 0 && r2 < p.rows)) pg = page_of(p.table, p.pages, r2, jj);
+                    }
+                    const int page = max(__shfl_sync(kFull, pg, 0), 0);
+                    const int pprev = __shfl_sync(kFull, pg, 1), pnext = __shfl_sync(kFull, pg, 2);
+                    const uint64_t ppol = (pprev == page || pnext == page) ? pol_shared : pol;
                     if (lane == 0) {
                         const int flags = seg_flags | (s == 0 ? kFlagFirst : 0) | (s == seg - 1 ? kFlagLast : 0) |
                                           ((s == 0 && append) ? kFlagHasLast : 0) |
@@ -693,14 +634,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                         const uint32_t fb = bar_full + 8 * st;
                         const uint32_t dst = base + st * kStageBytes;
                         uint32_t bytes = kStageBytes;
-                        if (s == 0) bytes += 1536 + (append ? 1024 : 0);
+                        if (s == 0) bytes += p.prepared ? 2048 : 1536 + (append ? 1024 : 0);
                         mbar_arrive_expect_tx(fb, bytes);
                         const int y = page * kPageSize;
-                        tma_load_3d(dst, &tmK, 0, y, g, fb, pol);
-                        tma_load_3d(dst + 8192, &tmK, 64, y, g, fb, pol);
-                        tma_load_3d(dst + 16384, &tmV, 0, y, g, fb, pol);
-                        tma_load_3d(dst + 24576, &tmV, 64, y, g, fb, pol);
-                        if (s == 0) {
+                        tma_load_3d(dst, &tmK, 0, y, g, fb, ppol);
+                        tma_load_3d(dst + 8192, &tmK, 64, y, g, fb, ppol);
+                        tma_load_3d(dst + 16384, &tmV, 0, y, g, fb, ppol);
+                        tma_load_3d(dst + 24576, &tmV, 64, y, g, fb, ppol);
+                        if (s == 0 && p.prepared) {  // the 4 heads' prepared q, fp32
+                            const uint32_t side = base + L::kSide + st * kSideBytes;
+                            bulk_copy(side, p.qhat + ((int64_t)t * H + g * kGroup) * kHeadDim, 2048, fb);
+                        } else if (s == 0) {
                             const uint32_t side = base + L::kSide + st * kSideBytes;
                             bulk_copy(side + kSideQ, p.q + ((int64_t)t * H + g * kGroup) * kHeadDim, 1024, fb);
                             bulk_copy(side + kSideRopeHi, p.rope_hi + (int64_t)pos * kRopeHalf, 512, fb);
@@ -732,296 +676,315 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
         if (ok) {  // the end: a ring item without data that stops the consumers
             const int st = i % kStages;
-            if (i >= kStages && (!mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1) || *abort_flag)) {
+            if (i >= kStages &&
+                __any_sync(kFull, !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1, p.wait_ns) || *abort_flag)) {
                 ok = false;
             } else if (lane == 0) {
                 sMeta[2 * st + 1] = make_int4(kFlagStop, 0, 0, 0);
                 mbar_arrive(bar_full + 8 * st);
+                *s_stop_sent = 1;
             }
             __syncwarp();
+        }
+        if (lane == 0) {
+            *s_issued = i;
+            if (!ok) {
+                atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else {
+
+        // ==================================================================== consumers
+        const int gid = lane >> 2, tig = lane & 3;
+        // This lane's B fragments hold dims 16ks + 2tig + {0, 1, 8, 9} (ks = 0..7) of
+        // one query head: 32 dims, closed under the rotate-half pairing (d, d +- 64),
+        // and the four lanes tig = 0..3 of a head hold all 128 of its dims.
+        const uint32_t* sWq = reinterpret_cast<const uint32_t*>(sW);  // q_norm_w as bf16 pairs
+        uint32_t wq2[8][2];  // q_norm weights of those dims, bf16 pairs
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int d0 = 16 * ks + 2 * tig;
+            wq2[ks][0] = sWq[d0 >> 1];
+            wq2[ks][1] = sWq[(d0 + 8) >> 1];
+        }
+        float wk[4];
+        unpack4(sW[32 + lane], wk);
+        const float qscale = 1.4426950408889634f * 0.088388347648318440f;  // log2(e) / sqrt(128)
+        const bool rem_lane = tig >= 2;  // this lane's S/O columns are the remainder columns
+        const int hh = gid & 3, prt = gid >> 2;
+        const int srcA = 4 * (2 * tig) + (hh >> 1) + 2 * prt;  // lanes holding P for the PV B fragment
+        const int srcB = srcA + 4;
+        const int r_ld = lane & 7, j_ld = lane >> 3;
+        uint32_t gphase = 0;
+
+        uint32_t bq[8][2];
+        float o[8][4];
+        float mA = -CUDART_INF_F, mB = -CUDART_INF_F, lA = 0.f, lB = 0.f;
+        uint2 knew = make_uint2(0u, 0u), vnew = make_uint2(0u, 0u);  // the row's new k (normed, roped) and v
+        bool ok = true;
+
+        for (int i = 0;; ++i) {
+            const int st = i % kStages;
+            if (__any_sync(kFull, !mbar_wait(bar_full + 8 * st, (i / kStages) & 1, p.wait_ns))) {
+                ok = false;
+                break;
+            }
+            const int4 m1 = sMeta[2 * st + 1];
+            const int flags = m1.x;
+            if (flags & kFlagStop) break;
+            const int4 m0 = sMeta[2 * st];
+            const int t = m0.x, g = m0.y, jj = m0.z, len = m0.w, pidx = m1.y, page = m1.z;
+            const uint32_t kb = base + st * kStageBytes;
+            const uint32_t vb = kb + 16384;
+
+            if ((flags & kFlagFirst) && p.prepared) {
+                q_from_hat(reinterpret_cast<const float*>(sbase + L::kSide + st * kSideBytes) + hh * kHeadDim, qscale,
+                           tig, prt, bq);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+                mA = mB = -CUDART_INF_F;
+                lA = lB = 0.f;
+            } else if (flags & kFlagFirst) {
+                const uint8_t* side = sbase + L::kSide + st * kSideBytes;
+                const float2* rpf = reinterpret_cast<const float2*>(side + kSideRopeHi);
+                // q of head 4g+hh, the dims of this lane's B fragments: QK-norm + RoPE in
+                // fp32 from the raw q and (cos, sin) staged with this page, scaled by
+                // log2(e)/sqrt(128), then split into bf16 head (cols 0-3) and remainder (cols 4-7)
+                {
+                    const uint8_t* qrow = side + hh * 256;
+                    uint32_t xr[8][2];
+                    float ss = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int d0 = 16 * ks + 2 * tig;
+                        xr[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 2 * d0);
+                        xr[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 2 * (d0 + 8));
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float a = __uint_as_float(xr[ks][e] << 16), b = __uint_as_float(xr[ks][e] & 0xffff0000u);
+                            ss += a * a + b * b;
+                        }
+                    }
+                    ss += __shfl_xor_sync(kFull, ss, 1);
+                    ss += __shfl_xor_sync(kFull, ss, 2);
+                    const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * qscale;
+                    switch (p.rot) {  // rotated dims: pairs (d, d + rot / 2)
+                    case 128: q_prep<4>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                    case 96: q_prep<3>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                    case 64: q_prep<2>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                    default: q_prep<1>(xr, wq2, rpf, inv, tig, prt, bq); break;
+                    }
+                }
+                // the warp that owns the new slot's position prepares the row's k and v
+                if ((flags & kFlagHasLast) && warp == ((len - 1) % kPageSize) / 16) {
+                    knew = norm_rope_k(*reinterpret_cast<const uint2*>(side + kSideK + 8 * lane), wk, rpf,
+                                       reinterpret_cast<const float2*>(side + kSideRopeLo), p.eps, lane, p.rot);
+                    vnew = *reinterpret_cast<const uint2*>(side + kSideV + 8 * lane);
+                }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+                mA = mB = -CUDART_INF_F;
+                lA = lB = 0.f;
+            }
+
+            if ((flags & kFlagAppend) && warp == ((len - 1) % kPageSize) / 16) {
+                // the page holding the row's new slot: write k and v into the staged
+                // page (row r of the 128-byte-swizzled halves) and into the pool
+                const int r = (len - 1) % kPageSize;
+                const int half = lane >> 4, chunk = (lane & 15) >> 1;
+                const uint32_t off = half * 8192 + r * 128 + ((chunk ^ (r & 7)) << 4) + (lane & 1) * 8;
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + off), "r"(knew.x), "r"(knew.y) : "memory");
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(vb + off), "r"(vnew.x), "r"(vnew.y) : "memory");
+                const int64_t slot = (int64_t)page * kPageSize + r;
+                const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane;
+                *reinterpret_cast<uint2*>(p.K + dst) = knew;
+                *reinterpret_cast<uint2*>(p.V + dst) = vnew;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
+                __syncwarp();
+            }
+
+            // ---- S = K q^T (two accumulators for ILP)
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int rowk = 16 * warp + r_ld + 8 * (j_ld & 1);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int cc = 2 * ks + (j_ld >> 1);
+                    const uint32_t addr = kb + (ks >> 2) * 8192 + rowk * 128 + (((cc & 7) ^ (rowk & 7)) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(addr, a0, a1, a2, a3);
+                    if (ks & 1)
+                        mma_bf16_16816(c1, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+                    else
+                        mma_bf16_16816(c0, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+                }
+            }
+            float sv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sv[k] = c0[k] + c1[k];
+                sv[k] += __shfl_xor_sync(kFull, sv[k], 2);  // head column + remainder column
+            }
+            // sv[0]: (pos gid, head A), sv[1]: (gid, B), sv[2]: (gid+8, A), sv[3]: (gid+8, B)
+            const int pbase = jj * kPageSize + 16 * warp;
+            if (pbase + gid >= len) sv[0] = sv[1] = -CUDART_INF_F;
+            if (pbase + gid + 8 >= len) sv[2] = sv[3] = -CUDART_INF_F;
+
+            float tA = fmaxf(sv[0], sv[2]), tB = fmaxf(sv[1], sv[3]);
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                tA = fmaxf(tA, __shfl_xor_sync(kFull, tA, o2));
+                tB = fmaxf(tB, __shfl_xor_sync(kFull, tB, o2));
+            }
+            const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+            const float aA = (nA == -CUDART_INF_F) ? 1.f : exp2f(mA - nA);
+            const float aB = (nB == -CUDART_INF_F) ? 1.f : exp2f(mB - nB);
+            float pv[4];
+            pv[0] = (sv[0] == -CUDART_INF_F) ? 0.f : exp2f(sv[0] - nA);
+            pv[1] = (sv[1] == -CUDART_INF_F) ? 0.f : exp2f(sv[1] - nB);
+            pv[2] = (sv[2] == -CUDART_INF_F) ? 0.f : exp2f(sv[2] - nA);
+            pv[3] = (sv[3] == -CUDART_INF_F) ? 0.f : exp2f(sv[3] - nB);
+            lA = lA * aA + pv[0] + pv[2];
+            lB = lB * aB + pv[1] + pv[3];
+            mA = nA;
+            mB = nB;
+            if (aA != 1.f || aB != 1.f) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[mt][0] *= aA;
+                    o[mt][1] *= aB;
+                    o[mt][2] *= aA;
+                    o[mt][3] *= aB;
+                }
+            }
+
+            // ---- P fragment: this lane provides head-or-remainder parts of its four p values
+            uint32_t w_even, w_odd;
+            {
+                __nv_bfloat16 e[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    __nv_bfloat16 hd, tl;
+                    split_bf16(pv[k], hd, tl);
+                    e[k] = rem_lane ? tl : hd;
+                }
+                w_even = pack_bf16(e[0], e[2]);  // head A at positions gid, gid+8
+                w_odd = pack_bf16(e[1], e[3]);   // head B
+            }
+            const uint32_t xae = __shfl_sync(kFull, w_even, srcA), xao = __shfl_sync(kFull, w_odd, srcA);
+            const uint32_t xbe = __shfl_sync(kFull, w_even, srcB), xbo = __shfl_sync(kFull, w_odd, srcB);
+            const uint32_t XA = (hh & 1) ? xao : xae;  // {P[2tig][col], P[2tig+8][col]}
+            const uint32_t XB = (hh & 1) ? xbo : xbe;  // {P[2tig+1][col], P[2tig+9][col]}
+            const uint32_t pb0 = __byte_perm(XA, XB, 0x5410);
+            const uint32_t pb1 = __byte_perm(XA, XB, 0x7632);
+
+            // ---- O^T += V^T P
+            {
+                const int rowv = 16 * warp + r_ld + 8 * (j_ld >> 1);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int cc = 2 * mt + (j_ld & 1);
+                    const uint32_t addr = vb + (mt >> 2) * 8192 + rowv * 128 + (((cc & 7) ^ (rowv & 7)) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+                    mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (!(flags & kFlagLast)) {
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            } else {
+                // ---- end of segment: merge the four warps in a fixed order, write the output or a partial.
+                // Each warp parks its unscaled O in the K rows of this stage that only it read
+                // (rows 16w..16w+15 of the first half: 2 KiB), its m and l in sM/sL.
+                float lAs = lA, lBs = lB;
+#pragma unroll
+                for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                    lAs += __shfl_xor_sync(kFull, lAs, o2);
+                    lBs += __shfl_xor_sync(kFull, lBs, o2);
+                }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) o[mt][k] += __shfl_xor_sync(kFull, o[mt][k], 2);
+                float* park = reinterpret_cast<float*>(sbase + st * kStageBytes);  // [4 warps][4 heads][128]
+                if (tig < 2) {
+                    const int hA = 2 * tig, hB = hA + 1;
+                    float* pa = park + (warp * 4 + hA) * kHeadDim;
+                    float* pb = park + (warp * 4 + hB) * kHeadDim;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const int d = 16 * mt + gid;
+                        pa[d] = o[mt][0];
+                        pb[d] = o[mt][1];
+                        pa[d + 8] = o[mt][2];
+                        pb[d + 8] = o[mt][3];
+                    }
+                    if (gid == 0) {
+                        sM[warp * 4 + hA] = mA;
+                        sM[warp * 4 + hB] = mB;
+                        sL[warp * 4 + hA] = lAs;
+                        sL[warp * 4 + hB] = lBs;
+                    }
+                }
+                if (!group_sync(bar_group, gphase, lane, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                {
+                    const int h = warp;  // thread -> (head h, dims 4*lane..4*lane+3)
+                    float M = -CUDART_INF_F;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sM[w * 4 + h]);
+                    float Ls = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {  // fixed order: the result is reproducible
+                        const float mw = sM[w * 4 + h];
+                        const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+                        Ls += f * sL[w * 4 + h];
+                        const float4 ow = *reinterpret_cast<const float4*>(park + (w * 4 + h) * kHeadDim + 4 * lane);
+                        y[0] += f * ow.x;
+                        y[1] += f * ow.y;
+                        y[2] += f * ow.z;
+                        y[3] += f * ow.w;
+                    }
+                    const float inv = 1.f / Ls;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) y[k] *= inv;
+                    const int qh = g * kGroup + h;
+                    if (flags & kFlagComplete) {
+                        if (!(flags & kFlagValid)) y[0] = y[1] = y[2] = y[3] = 0.f;
+                        *reinterpret_cast<uint2*>(p.out + ((int64_t)t * H + qh) * kHeadDim + 4 * lane) = pack4(y);
+                    } else {
+                        const int64_t ph = (int64_t)pidx * kGroup + h;
+                        *reinterpret_cast<float4*>(p.part_o + ph * kHeadDim + 4 * lane) =
+                            make_float4(y[0], y[1], y[2], y[3]);
+                        if (lane == 0) p.part_lse[ph] = M + log2f(Ls);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
+                if (!group_sync(bar_group, gphase, lane, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            }
         }
         if (!ok && lane == 0) {
             atomicOr(p.err, PKV_DEVERR_TIMEOUT);
             *abort_flag = 1;
-            // wait (bounded) for the copies still in flight before the CTA exits
-            for (int k2 = max(0, i - kStages); k2 < i; ++k2)
-                mbar_wait(bar_full + 8 * (k2 % kStages), (k2 / kStages) & 1);
-        }
-        return;
-    }
-
-    // ==================================================================== consumers
-    const int gid = lane >> 2, tig = lane & 3;
-    // This lane's B fragments hold dims 16ks + 2tig + {0, 1, 8, 9} (ks = 0..7) of
-    // one query head: 32 dims, closed under the rotate-half pairing (d, d +- 64),
-    // and the four lanes tig = 0..3 of a head hold all 128 of its dims.
-    const uint32_t* sWq = reinterpret_cast<const uint32_t*>(sW);  // q_norm_w as bf16 pairs
-    uint32_t wq2[8][2];  // q_norm weights of those dims, bf16 pairs
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const int d0 = 16 * ks + 2 * tig;
-        wq2[ks][0] = sWq[d0 >> 1];
-        wq2[ks][1] = sWq[(d0 + 8) >> 1];
-    }
-    float wk[4];
-    unpack4(sW[32 + lane], wk);
-    const float qscale = 1.4426950408889634f * 0.088388347648318440f;  // log2(e) / sqrt(128)
-    const bool rem_lane = tig >= 2;  // this lane's S/O columns are the remainder columns
-    const int hh = gid & 3, prt = gid >> 2;
-    const int srcA = 4 * (2 * tig) + (hh >> 1) + 2 * prt;  // lanes holding P for the PV B fragment
-    const int srcB = srcA + 4;
-    const int r_ld = lane & 7, j_ld = lane >> 3;
-    uint32_t gphase = 0;
-
-    uint32_t bq[8][2];
-    float o[8][4];
-    float mA = -CUDART_INF_F, mB = -CUDART_INF_F, lA = 0.f, lB = 0.f;
-    uint2 knew = make_uint2(0u, 0u), vnew = make_uint2(0u, 0u);  // the row's new k (normed, roped) and v
-    bool ok = true;
-
-    for (int i = 0;; ++i) {
-        const int st = i % kStages;
-        if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
-            ok = false;
-            break;
-        }
-        const int4 m1 = sMeta[2 * st + 1];
-        const int flags = m1.x;
-        if (flags & kFlagStop) break;
-        const int4 m0 = sMeta[2 * st];
-        const int t = m0.x, g = m0.y, jj = m0.z, len = m0.w, pidx = m1.y, page = m1.z;
-        const uint32_t kb = base + st * kStageBytes;
-        const uint32_t vb = kb + 16384;
-
-        if (flags & kFlagFirst) {
-            const uint8_t* side = sbase + L::kSide + st * kSideBytes;
-            const float2* rpf = reinterpret_cast<const float2*>(side + kSideRopeHi);
-            // q of head 4g+hh, the dims of this lane's B fragments: QK-norm + RoPE in
-            // fp32 from the raw q and (cos, sin) staged with this page, scaled by
-            // log2(e)/sqrt(128), then split into bf16 head (cols 0-3) and remainder (cols 4-7)
-            {
-                const uint8_t* qrow = side + hh * 256;
-                uint32_t xr[8][2];
-                float ss = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int d0 = 16 * ks + 2 * tig;
-                    xr[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 2 * d0);
-                    xr[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 2 * (d0 + 8));
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float a = __uint_as_float(xr[ks][e] << 16), b = __uint_as_float(xr[ks][e] & 0xffff0000u);
-                        ss += a * a + b * b;
-                    }
-                }
-                ss += __shfl_xor_sync(kFull, ss, 1);
-                ss += __shfl_xor_sync(kFull, ss, 2);
-                const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * qscale;
-                switch (p.rot) {  // rotated dims: pairs (d, d + rot / 2)
-                case 128: q_prep<4>(xr, wq2, rpf, inv, tig, prt, bq); break;
-                case 96: q_prep<3>(xr, wq2, rpf, inv, tig, prt, bq); break;
-                case 64: q_prep<2>(xr, wq2, rpf, inv, tig, prt, bq); break;
-                default: q_prep<1>(xr, wq2, rpf, inv, tig, prt, bq); break;
-                }
-            }
-            // the warp that owns the new slot's position prepares the row's k and v
-            if ((flags & kFlagHasLast) && warp == ((len - 1) % kPageSize) / 16) {
-                knew = norm_rope_k(*reinterpret_cast<const uint2*>(side + kSideK + 8 * lane), wk, rpf,
-                                   reinterpret_cast<const float2*>(side + kSideRopeLo), p.eps, lane, p.rot);
-                vnew = *reinterpret_cast<const uint2*>(side + kSideV + 8 * lane);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-            mA = mB = -CUDART_INF_F;
-            lA = lB = 0.f;
-        }
-
-        if ((flags & kFlagAppend) && warp == ((len - 1) % kPageSize) / 16) {
-            // the page holding the row's new slot: write k and v into the staged
-            // page (row r of the 128-byte-swizzled halves) and into the pool
-            const int r = (len - 1) % kPageSize;
-            const int half = lane >> 4, chunk = (lane & 15) >> 1;
-            const uint32_t off = half * 8192 + r * 128 + ((chunk ^ (r & 7)) << 4) + (lane & 1) * 8;
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(kb + off), "r"(knew.x), "r"(knew.y) : "memory");
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(vb + off), "r"(vnew.x), "r"(vnew.y) : "memory");
-            const int64_t slot = (int64_t)page * kPageSize + r;
-            const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane;
-            *reinterpret_cast<uint2*>(p.K + dst) = knew;
-            *reinterpret_cast<uint2*>(p.V + dst) = vnew;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
-            __syncwarp();
-        }
-
-        // ---- S = K q^T (two accumulators for ILP)
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            const int rowk = 16 * warp + r_ld + 8 * (j_ld & 1);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const int cc = 2 * ks + (j_ld >> 1);
-                const uint32_t addr = kb + (ks >> 2) * 8192 + rowk * 128 + (((cc & 7) ^ (rowk & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(addr, a0, a1, a2, a3);
-                if (ks & 1)
-                    mma_bf16_16816(c1, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
-                else
-                    mma_bf16_16816(c0, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
-            }
-        }
-        float sv[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            sv[k] = c0[k] + c1[k];
-            sv[k] += __shfl_xor_sync(kFull, sv[k], 2);  // head column + remainder column
-        }
-        // sv[0]: (pos gid, head A), sv[1]: (gid, B), sv[2]: (gid+8, A), sv[3]: (gid+8, B)
-        const int pbase = jj * kPageSize + 16 * warp;
-        if (pbase + gid >= len) sv[0] = sv[1] = -CUDART_INF_F;
-        if (pbase + gid + 8 >= len) sv[2] = sv[3] = -CUDART_INF_F;
-
-        float tA = fmaxf(sv[0], sv[2]), tB = fmaxf(sv[1], sv[3]);
-#pragma unroll
-        for (int o2 = 4; o2 < 32; o2 <<= 1) {
-            tA = fmaxf(tA, __shfl_xor_sync(kFull, tA, o2));
-            tB = fmaxf(tB, __shfl_xor_sync(kFull, tB, o2));
-        }
-        const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
-        const float aA = (nA == -CUDART_INF_F) ? 1.f : exp2f(mA - nA);
-        const float aB = (nB == -CUDART_INF_F) ? 1.f : exp2f(mB - nB);
-        float pv[4];
-        pv[0] = (sv[0] == -CUDART_INF_F) ? 0.f : exp2f(sv[0] - nA);
-        pv[1] = (sv[1] == -CUDART_INF_F) ? 0.f : exp2f(sv[1] - nB);
-        pv[2] = (sv[2] == -CUDART_INF_F) ? 0.f : exp2f(sv[2] - nA);
-        pv[3] = (sv[3] == -CUDART_INF_F) ? 0.f : exp2f(sv[3] - nB);
-        lA = lA * aA + pv[0] + pv[2];
-        lB = lB * aB + pv[1] + pv[3];
-        mA = nA;
-        mB = nB;
-        if (aA != 1.f || aB != 1.f) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= aA;
-                o[mt][1] *= aB;
-                o[mt][2] *= aA;
-                o[mt][3] *= aB;
-            }
-        }
-
-        // ---- P fragment: this lane provides head-or-remainder parts of its four p values
-        uint32_t w_even, w_odd;
-        {
-            __nv_bfloat16 e[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                __nv_bfloat16 hd, tl;
-                split_bf16(pv[k], hd, tl);
-                e[k] = rem_lane ? tl : hd;
-            }
-            w_even = pack_bf16(e[0], e[2]);  // head A at positions gid, gid+8
-            w_odd = pack_bf16(e[1], e[3]);   // head B
-        }
-        const uint32_t xae = __shfl_sync(kFull, w_even, srcA), xao = __shfl_sync(kFull, w_odd, srcA);
-        const uint32_t xbe = __shfl_sync(kFull, w_even, srcB), xbo = __shfl_sync(kFull, w_odd, srcB);
-        const uint32_t XA = (hh & 1) ? xao : xae;  // {P[2tig][col], P[2tig+8][col]}
-        const uint32_t XB = (hh & 1) ? xbo : xbe;  // {P[2tig+1][col], P[2tig+9][col]}
-        const uint32_t pb0 = __byte_perm(XA, XB, 0x5410);
-        const uint32_t pb1 = __byte_perm(XA, XB, 0x7632);
-
-        // ---- O^T += V^T P
-        {
-            const int rowv = 16 * warp + r_ld + 8 * (j_ld >> 1);
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int cc = 2 * mt + (j_ld & 1);
-                const uint32_t addr = vb + (mt >> 2) * 8192 + rowv * 128 + (((cc & 7) ^ (rowv & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-                mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-            }
-        }
-        __syncwarp();
-        if (!(flags & kFlagLast)) {
-            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
-        } else {
-            // ---- end of segment: merge the four warps in a fixed order, write the output or a partial.
-            // Each warp parks its unscaled O in the K rows of this stage that only it read
-            // (rows 16w..16w+15 of the first half: 2 KiB), its m and l in sM/sL.
-            float lAs = lA, lBs = lB;
-#pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                lAs += __shfl_xor_sync(kFull, lAs, o2);
-                lBs += __shfl_xor_sync(kFull, lBs, o2);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) o[mt][k] += __shfl_xor_sync(kFull, o[mt][k], 2);
-            float* park = reinterpret_cast<float*>(sbase + st * kStageBytes);  // [4 warps][4 heads][128]
-            if (tig < 2) {
-                const int hA = 2 * tig, hB = hA + 1;
-                float* pa = park + (warp * 4 + hA) * kHeadDim;
-                float* pb = park + (warp * 4 + hB) * kHeadDim;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    const int d = 16 * mt + gid;
-                    pa[d] = o[mt][0];
-                    pb[d] = o[mt][1];
-                    pa[d + 8] = o[mt][2];
-                    pb[d + 8] = o[mt][3];
-                }
-                if (gid == 0) {
-                    sM[warp * 4 + hA] = mA;
-                    sM[warp * 4 + hB] = mB;
-                    sL[warp * 4 + hA] = lAs;
-                    sL[warp * 4 + hB] = lBs;
-                }
-            }
-            if (!group_sync(bar_group, gphase, lane)) {
-                ok = false;
-                break;
-            }
-            {
-                const int h = warp;  // thread -> (head h, dims 4*lane..4*lane+3)
-                float M = -CUDART_INF_F;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sM[w * 4 + h]);
-                float Ls = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {  // fixed order: the result is reproducible
-                    const float mw = sM[w * 4 + h];
-                    const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
-                    Ls += f * sL[w * 4 + h];
-                    const float4 ow = *reinterpret_cast<const float4*>(park + (w * 4 + h) * kHeadDim + 4 * lane);
-                    y[0] += f * ow.x;
-                    y[1] += f * ow.y;
-                    y[2] += f * ow.z;
-                    y[3] += f * ow.w;
-                }
-                const float inv = 1.f / Ls;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) y[k] *= inv;
-                const int qh = g * kGroup + h;
-                if (flags & kFlagComplete) {
-                    if (!(flags & kFlagValid)) y[0] = y[1] = y[2] = y[3] = 0.f;
-                    *reinterpret_cast<uint2*>(p.out + ((int64_t)t * H + qh) * kHeadDim + 4 * lane) = pack4(y);
-                } else {
-                    const int64_t ph = (int64_t)pidx * kGroup + h;
-                    *reinterpret_cast<float4*>(p.part_o + ph * kHeadDim + 4 * lane) =
-                        make_float4(y[0], y[1], y[2], y[3]);
-                    if (lane == 0) p.part_lse[ph] = M + log2f(Ls);
-                }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before TMA refills this stage
-            if (!group_sync(bar_group, gphase, lane)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
         }
     }
-    if (!ok && lane == 0) {
-        atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-        *abort_flag = 1;
+    // Every role has stopped.  After an abort, copies of up to kStages ring items
+    // may still be landing in this CTA's shared memory: wait for them (with the
+    // full limit, whatever the call's wait limit) before the CTA exits.
+    __syncthreads();
+    if (tid == 0 && *abort_flag) {
+        const int n = *s_issued;
+        // the stop item, when sent, reused the stage of item n - kStages, which had landed
+        for (int k2 = max(0, n - kStages + (*s_stop_sent ? 1 : 0)); k2 < n; ++k2)
+            mbar_wait(bar_full + 8 * (k2 % kStages), (k2 / kStages) & 1, kWaitLimitNs);
     }
 }
 
@@ -1068,14 +1031,18 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.err = pool->err;
     p.ntok = plan.tokens;
     p.pages = a.pages;
+    p.rows = a.rows;
     p.num_pages = pool->num_pages;
     p.max_seq = pool->cfg.max_seq;
     p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.decode_mode = decode_mode ? 1 : 0;
+    p.qhat = a.q_hat;
+    p.prepared = a.q_hat ? 1 : 0;
     p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.num_slots = pool->num_slots;
     p.eps = static_cast<float>(pool->cfg.eps);
+    p.wait_ns = pool->wait_ns;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.ctas);

@@ -22,8 +22,11 @@
 // memory, in a fixed order) and writes it.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
+#include "pkv_rope.cuh"
 
 namespace pkv {
 
@@ -47,6 +50,28 @@ struct LinShape {
     static constexpr int kAlloc = kTmemSlot + 16 + 1024;
 };
 
+// The q/k/v projection with the per-token work before attention fused into
+// its epilogue (pkv_qkv_proj_append): each 128-feature tile is one head, so the
+// CTA that finishes a token's head of q, k or v holds all of it.  Token t is a
+// decode row (table row t) at positions[t]; qhat receives its QK-normed, roped
+// q in fp32, and its normed, roped k (bf16) and its v go straight to its slot
+// of the pool.  Rows the attention skips (position -1, or a position or page
+// it cannot read) are not written.
+struct LinFuse {
+    const __nv_bfloat16* qw;   // q_norm weights [128]
+    const __nv_bfloat16* kw;   // k_norm weights [128]
+    const int32_t* positions;  // [tokens]
+    const int32_t* table;      // [tokens][pages], or null: contiguous rows
+    const float2* rope_hi;     // (cos, sin) [max_seq][64]
+    const float2* rope_lo;
+    __nv_bfloat16* K;          // pool [kv_heads][num_slots][128]
+    __nv_bfloat16* V;
+    float* qhat;               // [tokens][heads][128]
+    int64_t num_slots;
+    int pages, num_pages, max_seq, rot, heads;
+    float eps;
+};
+
 // The output features split into up to three consecutive segments, each
 // written to its own [tokens][width] tensor (q, k, v of one fused projection);
 // segment boundaries are multiples of 128, so a tile lies in one segment.
@@ -55,7 +80,89 @@ struct LinParams {
     int seg_end[3];     // cumulative widths; seg_end[2] == out
     uint32_t* err;
     int tokens, in, out, splits;
+    int fused;          // 1: the epilogue of LinFuse instead of writing y
+    LinFuse f;
 };
+
+// Fused epilogue for tokens [t_lo, t_hi) of the tile (rows n0 + t): warp w takes
+// tokens t_lo + w, t_lo + w + 4, ...; lane l sums features 4l..4l+3 of the token
+// over the NS partial tiles [token][feature] fp32 at the cluster addresses src
+// (NS = 1: this CTA's own tile, plain shared memory), rounds them to bf16 -- the
+// projection's output, as the pages' q/k/v tensors are bf16 -- and does the
+// segment's work: q -> norm + rope -> qhat; k -> norm + rope -> K[slot]; v -> V[slot].
+template <int NS>
+__device__ __forceinline__ void fused_rows(const LinParams& p, const uint32_t (&src)[NS], const float* own,
+                                           int t_lo, int t_hi, int n0, int m0, int warp, int lane)
+{
+    const LinFuse& f = p.f;
+    const int seg = m0 < p.seg_end[0] ? 0 : (m0 < p.seg_end[1] ? 1 : 2);
+    const int head = (m0 - (seg ? p.seg_end[seg - 1] : 0)) / kBM;
+    const KRope kr = krope(lane, f.rot);
+    float w4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (seg < 2) unpack4(reinterpret_cast<const uint2*>(seg == 0 ? f.qw : f.kw)[lane], w4);
+    for (int t = t_lo + warp; t < t_hi; t += 4) {
+        const int tok = n0 + t;
+        if (tok >= p.tokens) break;  // the same for the whole warp
+        const int pos = f.positions[tok];
+        float4 a;
+        if (NS == 1) {
+            a = reinterpret_cast<const float4*>(own)[t * (kBM / 4) + lane];
+        } else {
+            float4 v[NS];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) v[q] = ld_cluster_f32x4(src[q] + (uint32_t)(t * kBM + 4 * lane) * 4);
+            a = v[0];
+#pragma unroll
+            for (int q = 1; q < NS; ++q) {
+                a.x += v[q].x;
+                a.y += v[q].y;
+                a.z += v[q].z;
+                a.w += v[q].w;
+            }
+        }
+        uint2 raw;
+        raw.x = pack_bf16(__float2bfloat16_rn(a.x), __float2bfloat16_rn(a.y));
+        raw.y = pack_bf16(__float2bfloat16_rn(a.z), __float2bfloat16_rn(a.w));
+        // the rows the attention would skip: position -1 (no step), out of range, or a page it cannot read
+        uint32_t e = 0;
+        if (pos != -1 && (pos < 0 || pos >= f.max_seq || pos >= f.pages * kPageSize)) e = PKV_DEVERR_POSITION;
+        int bad = 0;
+        if (pos >= 0 && !e)
+            for (int j = lane; j <= pos / kPageSize; j += 32) {
+                const int id = page_of(f.table, f.pages, tok, j);
+                bad |= (id < 0 || id >= f.num_pages);
+            }
+        if (__any_sync(kFull, bad)) e = PKV_DEVERR_PAGE;
+        if (pos == -1 || e) {
+            if (e && seg == 1 && head == 0 && lane == 0) atomicOr(p.err, e);
+            continue;
+        }
+        const int rf0 = kr.f0;
+        float2 rh[4], rl[4];
+        {
+            const float4* h4 = reinterpret_cast<const float4*>(f.rope_hi + (int64_t)pos * kRopeHalf + rf0);
+            const float4 h0 = h4[0], h1 = h4[1];
+            rh[0] = make_float2(h0.x, h0.y), rh[1] = make_float2(h0.z, h0.w), rh[2] = make_float2(h1.x, h1.y),
+            rh[3] = make_float2(h1.z, h1.w);
+        }
+        if (seg == 0) {
+            *reinterpret_cast<float4*>(f.qhat + ((int64_t)tok * f.heads + head) * kHeadDim + 4 * lane) =
+                norm_rope_q_regs(raw, w4, rh, f.eps, lane, f.rot);
+            continue;
+        }
+        const int64_t slot = (int64_t)page_of(f.table, f.pages, tok, pos / kPageSize) * kPageSize + pos % kPageSize;
+        const int64_t dst = ((int64_t)head * f.num_slots + slot) * kHeadDim + 4 * lane;
+        if (seg == 1) {
+            const float4* l4 = reinterpret_cast<const float4*>(f.rope_lo + (int64_t)pos * kRopeHalf + rf0);
+            const float4 l0 = l4[0], l1 = l4[1];
+            rl[0] = make_float2(l0.x, l0.y), rl[1] = make_float2(l0.z, l0.w), rl[2] = make_float2(l1.x, l1.y),
+            rl[3] = make_float2(l1.z, l1.w);
+            *reinterpret_cast<uint2*>(f.K + dst) = norm_rope_k_regs(raw, w4, rh, rl, f.eps, lane, f.rot);
+        } else {
+            *reinterpret_cast<uint2*>(f.V + dst) = raw;  // v is written as given
+        }
+    }
+}
 
 // The segment holding output tile row m0: its tensor, its width and the tile's column in it.
 __device__ __forceinline__ __nv_bfloat16* seg_of(const LinParams& p, int m0, int& width, int& col)
@@ -200,6 +307,29 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
     int yw, yc;
     __nv_bfloat16* const y = seg_of(p, m0, yw, yc);
     const int o = yc + 32 * warp + lane;  // this thread's column of y
+    if (p.splits == 1 && p.fused) {
+        // stage the tile [token][feature] in the idle ring, then the token-major fused epilogue
+        float* part = reinterpret_cast<float*>(sbase);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
+            tmem_wait_ld_regs(v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) part[(c0 + j) * kBM + 32 * warp + lane] = ok ? __uint_as_float(v[j]) : 0.f;
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, BN);
+        }
+        if (ok) {
+            const uint32_t none[1] = {0u};
+            fused_rows<1>(p, none, part, 0, BN, n0, m0, warp, lane);
+        }
+        return;
+    }
     if (p.splits == 1) {
         if (ok) {
 #pragma unroll 1
@@ -240,6 +370,22 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
     }
     const uint32_t local = smem_u32(part);
     const int r = (int)cluster_rank();
+    if (p.fused) {  // CTA r of the cluster finishes tokens [r BN / NS, (r + 1) BN / NS) of the tile
+        auto run = [&](auto ns_tag) {
+            constexpr int NS = decltype(ns_tag)::value;
+            uint32_t src[NS];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) src[q] = cluster_map(local, q);
+            fused_rows<NS>(p, src, part, r * BN / NS, (r + 1) * BN / NS, n0, m0, warp, lane);
+        };
+        switch (p.splits) {
+        case 2: run(std::integral_constant<int, 2>{}); break;
+        case 4: run(std::integral_constant<int, 4>{}); break;
+        default: run(std::integral_constant<int, 8>{}); break;
+        }
+        cluster_sync();
+        return;
+    }
     switch (p.splits) {  // linear_splits gives 2, 4 or 8
     case 2: cluster_reduce<BN, 2>(local, r, tid, n0, p.tokens, y, yw, yc); break;
     case 4: cluster_reduce<BN, 4>(local, r, tid, n0, p.tokens, y, yw, yc); break;
@@ -260,7 +406,7 @@ cudaError_t launch_linear_bn(pkv_pool* pool, const void* x, const void* w, const
     cudaError_t e = cudaFuncSetAttribute(linear_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
     if (e != cudaSuccess) return e;
     const bool timed = pool->timer_on;
-    const int slot = (int)(pool->timer_count % kTimerSlots);
+    const int slot = timed ? (int)(pool->timer_count.fetch_add(1) % kTimerSlots) : 0;
     if (timed && (e = cudaEventRecord(pool->ev_start[slot], s)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.out / kBM, (p.tokens + BN - 1) / BN, splits);
@@ -278,10 +424,7 @@ cudaError_t launch_linear_bn(pkv_pool* pool, const void* x, const void* w, const
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, linear_kernel<BN>, tmW, tmX, p);
     if (e != cudaSuccess) return e;
-    if (timed) {
-        if ((e = cudaEventRecord(pool->ev_stop[slot], s)) != cudaSuccess) return e;
-        pool->timer_count++;
-    }
+    if (timed && (e = cudaEventRecord(pool->ev_stop[slot], s)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
@@ -302,10 +445,23 @@ int linear_splits(const pkv_pool* pool, int tokens, int in, int out)
     return splits;
 }
 
+static cudaError_t launch_linear_p(pkv_pool* pool, const void* x, const void* w, LinParams& p, cudaStream_t s)
+{
+    p.splits = linear_splits(pool, p.tokens, p.in, p.out);
+    switch (linear_tile_tokens(p.tokens)) {
+    case 64:
+        return launch_linear_bn<64>(pool, x, w, p, p.splits, s);
+    case 128:
+        return launch_linear_bn<128>(pool, x, w, p, p.splits, s);
+    default:
+        return launch_linear_bn<256>(pool, x, w, p, p.splits, s);
+    }
+}
+
 cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, int tokens, int in, int nseg,
                           void* const* y, const int* widths, cudaStream_t s)
 {
-    LinParams p;
+    LinParams p = {};
     int end = 0;
     for (int i = 0; i < 3; ++i) {
         end += i < nseg ? widths[i] : 0;
@@ -316,15 +472,40 @@ cudaError_t launch_linear(pkv_pool* pool, const void* x, const void* w, int toke
     p.tokens = tokens;
     p.in = in;
     p.out = end;
-    p.splits = linear_splits(pool, tokens, in, end);
-    switch (linear_tile_tokens(tokens)) {
-    case 64:
-        return launch_linear_bn<64>(pool, x, w, p, p.splits, s);
-    case 128:
-        return launch_linear_bn<128>(pool, x, w, p, p.splits, s);
-    default:
-        return launch_linear_bn<256>(pool, x, w, p, p.splits, s);
-    }
+    p.fused = 0;
+    return launch_linear_p(pool, x, w, p, s);
+}
+
+cudaError_t launch_qkv_append(pkv_pool* pool, const void* x, const void* w_qkv, int tokens, int hidden,
+                              const QkvAppend& a, cudaStream_t s)
+{
+    LinParams p = {};
+    const int qw = pool->cfg.heads * kHeadDim, kw = pool->cfg.kv_heads * kHeadDim;
+    p.seg_end[0] = qw;
+    p.seg_end[1] = qw + kw;
+    p.seg_end[2] = qw + 2 * kw;
+    p.err = pool->err;
+    p.tokens = tokens;
+    p.in = hidden;
+    p.out = p.seg_end[2];
+    p.fused = 1;
+    p.f.qw = static_cast<const __nv_bfloat16*>(a.q_norm_w);
+    p.f.kw = static_cast<const __nv_bfloat16*>(a.k_norm_w);
+    p.f.positions = a.positions;
+    p.f.table = a.table;
+    p.f.rope_hi = pool->rope_hi;
+    p.f.rope_lo = pool->rope_lo;
+    p.f.K = static_cast<__nv_bfloat16*>(pool->k);
+    p.f.V = static_cast<__nv_bfloat16*>(pool->v);
+    p.f.qhat = a.q_hat;
+    p.f.num_slots = pool->num_slots;
+    p.f.pages = a.pages;
+    p.f.num_pages = pool->num_pages;
+    p.f.max_seq = pool->cfg.max_seq;
+    p.f.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
+    p.f.heads = pool->cfg.heads;
+    p.f.eps = static_cast<float>(pool->cfg.eps);
+    return launch_linear_p(pool, x, w_qkv, p, s);
 }
 
 }  // namespace pkv

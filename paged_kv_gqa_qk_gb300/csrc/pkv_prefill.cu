@@ -552,12 +552,16 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
                         if (96 + k > lim) v3[k] = __float_as_uint(-CUDART_INF_F);
                     }
                 }
+                // row max, two new values per three-input max, four independent chains
                 float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    mx4[k & 3] = fmaxf(mx4[k & 3], fmaxf(fmaxf(__uint_as_float(v0[k]), __uint_as_float(v1[k])),
-                                                         fmaxf(__uint_as_float(v2[k]), __uint_as_float(v3[k]))));
-                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                for (int k = 0; k < 32; k += 2) {
+                    mx4[0] = fmax3(mx4[0], __uint_as_float(v0[k]), __uint_as_float(v0[k + 1]));
+                    mx4[1] = fmax3(mx4[1], __uint_as_float(v1[k]), __uint_as_float(v1[k + 1]));
+                    mx4[2] = fmax3(mx4[2], __uint_as_float(v2[k]), __uint_as_float(v2[k + 1]));
+                    mx4[3] = fmax3(mx4[3], __uint_as_float(v3[k]), __uint_as_float(v3[k + 1]));
+                }
+                const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
                 // move the running max (rescaling O and l) only when this block raises it by > 8
                 bool need = false;
                 float alpha = 1.f;
@@ -592,14 +596,18 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
                 // P = 2^(S - m) as bf16 pairs over the first half of S (a row with no key
                 // yet has m = -inf: its p are all 0)
                 const float msub = m_used == -CUDART_INF_F ? 0.f : m_used;
-                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                // per pair of keys: one paired subtract, two exp2, one paired add to the
+                // row sum, one paired conversion
+                const uint64_t negm2 = f2_pack(-msub, -msub);
+                uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};  // (+0.f, +0.f) pairs
                 auto p_chunk = [&](const uint32_t (&v)[32], int cc) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float a = ex2_approx(__uint_as_float(v[e]) - msub);
-                        const float bb = ex2_approx(__uint_as_float(v[e + 1]) - msub);
-                        ps4[(e >> 1) & 3] += a + bb;
+                        float x0, x1;
+                        f2_unpack(f2_add(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), negm2), x0, x1);
+                        const float a = ex2_approx(x0), bb = ex2_approx(x1);
+                        ps2[(e >> 1) & 3] = f2_add(ps2[(e >> 1) & 3], f2_pack(a, bb));
                         const __nv_bfloat162 ab = __floats2bfloat162_rn(a, bb);  // one paired conversion
                         pk[e / 2] = *reinterpret_cast<const uint32_t*>(&ab);
                     }
@@ -609,7 +617,12 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
                 p_chunk(v1, 1);
                 p_chunk(v2, 2);
                 p_chunk(v3, 3);
-                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                {
+                    float s[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) f2_unpack(ps2[k], s[2 * k], s[2 * k + 1]);
+                    l += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -815,7 +828,7 @@ cudaError_t configure_prefill()
     return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem::kAlloc);
 }
 
-cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
+cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, cudaStream_t s)
 {
     PfParams p;
     p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -835,8 +848,9 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.eps = static_cast<float>(pool->cfg.eps);
     const int units = p.ntiles * p.kv_heads;
+    const int grid = ctas < units ? ctas : units;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units < pool->num_sms ? units : pool->num_sms));
+    cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
     cfg.blockDim = dim3(kPfThreads);
     cfg.dynamicSmemBytes = PfSmem::kAlloc;
     cfg.stream = s;

@@ -55,32 +55,49 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // every wait gives up after one second
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // default limit of every wait: one second
 
 // Bounded wait for the phase with the given parity to complete, sleeping
-// between polls (for waits on copies from memory).  Gives up after a second
-// and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// between polls (for waits on copies from memory).  Gives up after limit_ns
+// and returns false; a limit of 0 gives up at once if the phase is still open
+// (one non-blocking probe).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         __nanosleep(128);
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 
 // Bounded wait without sleeping, for short waits among the warps of one CTA
 // (try_wait itself suspends the thread for a while when the phase is open).
-// Gives up after a second and returns false.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
+// Gives up after limit_ns and returns false (0: one non-blocking probe).
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 1023u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 1023u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -293,6 +310,31 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- paired fp32 arithmetic (sm_100+): two lanes of work per instruction ----------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)

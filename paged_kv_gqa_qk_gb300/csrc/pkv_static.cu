@@ -15,15 +15,23 @@ __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTE
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device; null until set up
+void* g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device, from the last lookup
 
-// Device address of the scratch array on `dev` (the current device).  Looked
-// up once per device, on that device's first call.
-int scratch_address(int dev, void** out)
+// Device address of the scratch array on `dev` (the current device).  It is
+// looked up afresh on every call whose stream is not being captured (so a
+// module reloaded after cudaDeviceReset is seen); a call under stream capture
+// uses the address the last uncaptured call on that device found, and looks it
+// up only if there is none yet.
+int scratch_address(int dev, cudaStream_t stream, void** out)
 {
     if (dev < 0 || dev >= kMaxDevices) return PKV_EDEVICE;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        cs = cudaStreamCaptureStatusActive;  // unknown: do not touch the module
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess || !p) {
@@ -44,6 +52,7 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
                                  const void* k_norm_w, const int32_t* positions, const int32_t* table, int rows,
                                  int pages, void* out, void* stream)
 {
+    pkv::NvtxRange range("pkv_decode_static");
     if (!pool || !q || !k || !v || !q_norm_w || !k_norm_w || !positions || !out) return PKV_EINVAL;
     if (rows <= 0 || pages <= 0) return PKV_EINVAL;
     if (rows > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
@@ -56,10 +65,14 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
     void* scratch = nullptr;
-    const int rc = scratch_address(dev, &scratch);
+    const int rc = scratch_address(dev, static_cast<cudaStream_t>(stream), &scratch);
     if (rc != PKV_OK) return rc;
 
     const pkv::StepArgs a = {q, k, v, q_norm_w, k_norm_w, nullptr, nullptr, nullptr, positions, table,
                              0, rows, pages, rows, out, static_cast<char*>(scratch)};
+    if (pkv::check_enabled()) {  // the same debugging pre-check as pkv_decode (host memory only)
+        const int pc = pkv::host_precheck(pool, a, static_cast<cudaStream_t>(stream));
+        if (pc != PKV_OK) return pc;
+    }
     return pkv::enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
 }

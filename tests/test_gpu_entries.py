@@ -153,3 +153,55 @@ def test_host_precheck_rejects_bad_slots(monkeypatch):
     pool.step(q, k, v, qw, kw, pos, prow, None, sp2.to(dev), tab2.to(dev), out=out)
     torch.cuda.synchronize()
     pool.close()
+
+
+def test_host_precheck_rejects_decode_rows_reading_another_rows_new_slot(monkeypatch):
+    """Decode orders each row's write before its own reads only, so with
+    PKV_CHECK=1 a decode call in which a row reads (at a position up to its
+    own) a slot another row writes is refused, through both decode entries;
+    a shared prefix (pages strictly before every sharing row's write page) is
+    accepted, and pkv_step, which orders every write before every read,
+    accepts the call the decode entries refuse and matches the oracle."""
+    monkeypatch.setenv("PKV_CHECK", "1")
+    wl = W.make_decode("cross reads", [100, 200], seed=40, table_pages=4)
+    dev = torch.device("cuda")
+    q, k, v, qw, kw, sp = (t.to(dev) for t in (wl.q, wl.k, wl.v, wl.q_norm_w, wl.k_norm_w, wl.step_positions))
+
+    def refused(table):
+        K, V = wl.K0.to(dev), wl.V0.to(dev)
+        pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+        out = torch.zeros_like(q)
+        tab = torch.as_tensor(table).to(dev)
+        with pytest.raises(pkv.PkvError) as ei:
+            pool.decode(q, k, v, qw, kw, sp, tab, out=out)
+        assert ei.value.code == pkv.PKV_EINVAL
+        with pytest.raises(pkv.PkvError) as ei:
+            pkv.pkv_decode_static(pool.handle, q, k, v, qw, kw, sp, tab, out)
+        assert ei.value.code == pkv.PKV_EINVAL
+        torch.cuda.synchronize()
+        assert not out.any() and torch.equal(K.cpu(), wl.K0) and torch.equal(V.cpu(), wl.V0)
+        pool.close()
+
+    # row 0 writes at page 1, offset 35; row 1 (position 199) reads all of its page 1
+    t1 = wl.table.clone()
+    t1[1, 1] = t1[0, 1]
+    refused(t1)
+    # the other direction: row 1's last page is row 0's write page, row 1 writes
+    # offset 20 of it, which row 0 (offset 35) reads
+    wl2 = W.make_decode("cross reads 2", [100, 85], seed=41, table_pages=4)
+    assert wl2.meta["lengths"] == [100, 85]
+    t2 = wl2.table.clone()
+    t2[1, 1] = t2[0, 1]
+    wl, q, k, v, qw, kw, sp = (wl2, *(t.to(dev) for t in (wl2.q, wl2.k, wl2.v, wl2.q_norm_w, wl2.k_norm_w,
+                                                          wl2.step_positions)))
+    refused(t2)
+    # a shared prefix page (page 0, before both write pages) passes and matches the oracle
+    t3 = wl.table.clone()
+    t3[1, 0] = t3[0, 0]
+    compare(wl, run_gpu(wl, table=t3), run_oracle(wl, table=t3), label="checked shared prefix")
+    # the same rows as a step (one prompt token stands in for P > 0): writes come first, so it is accepted
+    st = W.make_step("cross reads as a step", prompt_lengths=[1], prompt_starts=[0], decode_lengths=[100, 85],
+                     seed=42, table_pages=4)
+    t4 = st.table.clone()
+    t4[1, 1] = t4[0, 1]
+    compare(st, run_gpu(st, table=t4), run_oracle(st, table=t4), label="checked step cross reads")
