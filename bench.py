@@ -200,9 +200,11 @@ def measured_peak_bf16():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the decode attention kernel's sources (the kernel file and the headers it includes)."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "paged_kv_gqa_qk_gb300", "csrc", "pkv_kernels.cu"), "rb") as f:
-        h.update(f.read())
+    for name in ("pkv_kernels.cu", "pkv_rope.cuh", "pkv_ptx.cuh", "pkv_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_gqa_qk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -214,9 +216,11 @@ def ncu_traffic(workload: str):
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_sha") != kernel_source_hash() or d.get("workload") != workload:
-        return None
-    return d.get("dram_bytes_per_launch")
+    sha = kernel_source_hash()
+    for e in d.get("entries", []):
+        if e.get("kernel_sha") == sha and e.get("workload") == workload:
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 def prefill_algorithmic_flops(wl) -> int:
