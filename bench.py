@@ -14,7 +14,7 @@ clocks are sampled, and its median per-step time is reported beside
 ms_per_step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload config4|config2|config3|config5|sweepRxL|prefill|rows|linear_decode|linear_prefill]
+                  [--workload config4|config2|config3|config5|sweepRxL|prefill|rows|linear_decode|linear_prefill|layer]
                   [--sustain-seconds S]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
 
@@ -640,6 +640,149 @@ def run_gpu_linear(args) -> None:
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------- one attention layer
+
+def run_gpu_layer(args) -> None:
+    """One decode step of a whole attention layer over the 64-row batch (context
+    U[512,4096]) at Qwen3-8B's hidden size 4096, on synthetic weights: the q/k/v
+    projection with QK-norm, RoPE and the k/v append in its epilogue
+    (pkv_qkv_proj_append), the attention over the pool it wrote
+    (pkv_decode_appended) and o_proj (pkv_linear) -- 3 launches of ours plus
+    the attention's combine.  The same step through the unfused entries
+    (pkv_qkv_proj, pkv_decode, pkv_linear) is timed beside it."""
+    import torch
+    import paged_kv_gqa_qk_gb300 as pkv
+    import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    pkv.load_library()
+    wl = make_workload("config2", rank)
+    R, pages = wl.R, wl.pages
+    K, V = wl.K0.to(dev), wl.V0.to(dev)
+    pool = pkv.PagedKVPool(K, V, cfg=wl.cfg)
+    hidden = 4096
+    host_x, _ = W.make_linear(R, hidden, 128, seed=rank_seed(3200, rank))
+    w_qkv = W.make_linear(1, hidden, 6144, seed=rank_seed(3201, rank))[1].to(dev)
+    w_o = W.make_linear(1, hidden, hidden, seed=rank_seed(3202, rank))[1].to(dev)
+    x = host_x.to(dev)
+    qw, kw, pos, tab = (t.to(dev) for t in (wl.q_norm_w, wl.k_norm_w, wl.step_positions, wl.table))
+    q_hat = torch.empty(R, 32, 128, dtype=torch.float32, device=dev)
+    attn = torch.empty(R, 32, 128, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(R, hidden, dtype=torch.bfloat16, device=dev)
+    q, k, v = (torch.empty(R, h, 128, dtype=torch.bfloat16, device=dev) for h in (32, 8, 8))
+    ws = pool.workspace(R, pages, 0)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step_fused():
+        pkv.pkv_qkv_proj_append(pool.handle, x, w_qkv, qw, kw, pos, tab, q_hat, stream)
+        pkv.pkv_decode_appended(pool.handle, q_hat, pos, tab, attn, ws, stream)
+        pkv.pkv_linear(pool.handle, attn.view(R, hidden), w_o, y, None, stream)
+
+    def step_unfused():
+        pkv.pkv_qkv_proj(pool.handle, x, w_qkv, q, k, v, stream)
+        pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, attn, ws, stream)
+        pkv.pkv_linear(pool.handle, attn.view(R, hidden), w_o, y, None, stream)
+
+    def timed(step, n):
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                step()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step_fused()
+            step_unfused()
+    stream.synchronize()
+    if pkv.pkv_check_errors(pool.handle, stream):
+        raise SystemExit("device error flags")
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms_step = max_over_ranks(timed(step_fused, args.steps), world)
+        ms_unfused = max_over_ranks(timed(step_unfused, args.steps), world)
+        pkv.pkv_timer_enable(pool.handle, 2)   # events around the attention launch only
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                step_fused()
+        stream.synchronize()
+        attn_ms, attn_n = pkv.pkv_timer_read(pool.handle)
+        pkv.pkv_timer_enable(pool.handle, False)
+        sustained = sustained_pass(step_fused, None, stream, ms_step, args.sustain_seconds)
+    barrier(world)
+
+    host_in = host_x.pin_memory()
+    host_out = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            x.copy_(host_in, non_blocking=True)
+            step_fused()
+            host_out.copy_(y, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    if pkv.pkv_check_errors(pool.handle, stream):
+        raise SystemExit("device error flags")
+
+    S = wl.cfg["page_size"]
+    L = [int(p) + 1 for p in wl.step_positions.tolist()]
+    kv = W.kv_bytes_per_position(wl.cfg) * sum(L)
+    attn_bytes = kv + 4 * sum(-(-n // S) for n in L) + R * (32 * 128 * 4 + 32 * 128 * 2)  # K/V, table, q_hat, out
+    attn_s = attn_ms / 1e3 / max(attn_n, 1)
+    peak, peak_kind = measured_peak_hbm()
+    weight_bytes = 2 * hidden * (6144 + hidden)
+    res = {
+        "metric": METRIC,
+        "value": R * world / (ms_step / 1e3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 activations and cache, N(0,1/4096) bf16 weights, shuffled pages)",
+        "config": {"workload": "attention layer decode step, 64 rows x U[512,4096], hidden 4096: q/k/v projection "
+                               "with norm, RoPE and append fused, attention, o_proj",
+                   "rows": R, "hidden": hidden, "table_pages": pages, "sum_context": sum(L),
+                   "bytes_per_step": {"kv": kv, "weights": weight_bytes},
+                   "l2": f"inputs larger than L2: {(kv + weight_bytes) / 1e9:.2f} GB of K/V and weights per step",
+                   "parallelism": f"dp{world} (independent replicas)"},
+        "unfused_ms_per_step": ms_unfused,
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel", "achieved": attn_bytes / attn_s / 1e9, "peak": peak,
+                     "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s",
+                     "frac": attn_bytes / attn_s / 1e9 / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": attn_bytes, "avg_launch_us": attn_s * 1e6,
+                     "timed_launches": attn_n,
+                     "timing": "CUDA events around each attention launch, a separate pass of the same steps"},
+        "layer_gbs": (kv + weight_bytes) / (ms_step / 1e3) / 1e9,
+        "e2e": {"value": R * args.steps * world / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": host_in.numel() * 2,
+                "d2h_bytes_per_step": host_out.numel() * 2},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+        "sustained": sustained,
+    }
+    pool.close()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------------------- the oracle (CPU)
 
 def _oracle_step(wl, rows, K, V, args_bits, nthreads):
@@ -743,6 +886,8 @@ def main(argv=None):
         run_reference(args)
     elif args.workload.startswith("linear"):
         run_gpu_linear(args)
+    elif args.workload == "layer":
+        run_gpu_layer(args)
     else:
         run_gpu(args)
 

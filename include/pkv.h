@@ -410,7 +410,9 @@ PKV_API int pkv_set_wait_limit(pkv_pool* pool, int64_t ns);
  * pkv_linear around its matrix-product kernel.  pkv_timer_read synchronises on the last recorded event,
  * returns the summed duration in milliseconds and the number of timed
  * launches since the timer was last enabled, and keeps the timer running.
- * At most 4096 launches are kept (later ones overwrite the oldest).  Host
+ * At most 4096 launches are kept (later ones overwrite the oldest).
+ * enable: 0 off, 1 every launch named above, 2 the attention launches only
+ * (not pkv_linear / pkv_qkv_proj / pkv_qkv_proj_append); PKV_EINVAL otherwise.  Host
  * threads sharing a pool take distinct event slots; pkv_timer_enable and
  * pkv_timer_read should not race with calls in flight on other threads. */
 PKV_API int pkv_timer_enable(pkv_pool* pool, int enable);

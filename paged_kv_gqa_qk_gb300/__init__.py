@@ -318,8 +318,9 @@ def pkv_set_wait_limit(pool, ns: int) -> None:
     _check(load_library().pkv_set_wait_limit(pool, int(ns)), "pkv_set_wait_limit")
 
 
-def pkv_timer_enable(pool, enable: bool) -> None:
-    _check(load_library().pkv_timer_enable(pool, 1 if enable else 0), "pkv_timer_enable")
+def pkv_timer_enable(pool, enable) -> None:
+    """enable: False/0 off, True/1 every timed launch, 2 the attention launches only."""
+    _check(load_library().pkv_timer_enable(pool, int(enable)), "pkv_timer_enable")
 
 
 def pkv_timer_read(pool):

@@ -68,7 +68,7 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
 int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
 {
     const bool decode = a.P == 0;
-    const bool timed = pool->timer_on;
+    const bool timed = pool->timer_on != 0;
     const int slot = timed ? (int)(pool->timer_count.fetch_add(1) % kTimerSlots) : 0;
     if (!decode && a.steps == 0) {  // prompts only: prep -> prompt-token attention (the timed kernel)
         if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
@@ -653,7 +653,8 @@ int pkv_timer_enable(pkv_pool* pool, int enable)
                 return PKV_ECUDA;
         }
     }
-    pool->timer_on = enable != 0;
+    if (enable < 0 || enable > 2) return PKV_EINVAL;
+    pool->timer_on = enable;
     pool->timer_count = 0;
     return PKV_OK;
 }

@@ -53,7 +53,7 @@ struct pkv_pool {
     uint64_t wait_ns;      // limit of the decode attention kernel's ring and group waits (default 1 s)
     // kernel timer: a timed call takes event slot timer_count++ % kTimerSlots (atomic,
     // so host threads sharing the pool take distinct slots)
-    bool timer_on;
+    int timer_on;          // 0 off, 1 every timed launch, 2 the attention launches only
     std::atomic<int64_t> timer_count;
     cudaEvent_t* ev_start;
     cudaEvent_t* ev_stop;

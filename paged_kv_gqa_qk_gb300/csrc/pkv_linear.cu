@@ -47,7 +47,8 @@ struct LinShape {
     static_assert(kStages * kStageBytes >= kBM * BN * 4, "the ring holds the fp32 partial tile");
     static constexpr int kBars = kStages * kStageBytes;  // full[S], empty[S], done
     static constexpr int kTmemSlot = kBars + 8 * (2 * kStages + 1);
-    static constexpr int kAlloc = kTmemSlot + 16 + 1024;
+    static constexpr int kTok = (kTmemSlot + 16 + 15) / 16 * 16;  // fused epilogue: int2 (position, slot) per token
+    static constexpr int kAlloc = kTok + 8 * BN + 1024;
 };
 
 // The q/k/v projection with the per-token work before attention fused into
@@ -84,15 +85,61 @@ struct LinParams {
     LinFuse f;
 };
 
-// Fused epilogue for tokens [t_lo, t_hi) of the tile (rows n0 + t): warp w takes
-// tokens t_lo + w, t_lo + w + 4, ...; lane l sums features 4l..4l+3 of the token
+// The tokens of the tile this CTA finishes in the fused epilogue: all BN
+// without a split, tokens [r BN / NS, (r + 1) BN / NS) for CTA r of a cluster of NS.
+__device__ __forceinline__ void fused_token_range(const LinParams& p, int bn, int& t_lo, int& t_hi)
+{
+    const int ns = p.splits, r = ns > 1 ? (int)cluster_rank() : 0;
+    t_lo = r * bn / ns;
+    t_hi = (r + 1) * bn / ns;
+}
+
+// Run by warps 2 and 3 while the product runs: for each token t of the range,
+// tok[t - t_lo] = (position, slot), or position -1 for a token nothing is
+// written for -- no step (-1), a position out of range or a page the attention
+// cannot read (these set the error bits, from the CTAs of k's first head) --
+// and for rows past the batch.
+__device__ __forceinline__ void fused_tokens(const LinParams& p, int2* tok, int bn, int n0, int m0, int w2, int lane)
+{
+    const LinFuse& f = p.f;
+    int t_lo, t_hi;
+    fused_token_range(p, bn, t_lo, t_hi);
+    const bool reporter = m0 == p.seg_end[0];  // the tile of k's head 0
+    for (int t = t_lo + w2; t < t_hi; t += 2) {
+        const int tk = n0 + t;
+        int pos = tk < p.tokens ? f.positions[tk] : -1;
+        uint32_t e = 0;
+        if (pos != -1 && (pos < 0 || pos >= f.max_seq || pos >= f.pages * kPageSize)) e = PKV_DEVERR_POSITION;
+        int bad = 0;
+        if (pos >= 0 && !e)
+            for (int j = lane; j <= pos / kPageSize; j += 32) {
+                const int id = page_of(f.table, f.pages, tk, j);
+                bad |= (id < 0 || id >= f.num_pages);
+            }
+        if (__any_sync(kFull, bad)) e = PKV_DEVERR_PAGE;
+        int slot = 0;
+        if (e || pos < 0)
+            pos = -1;
+        else
+            slot = page_of(f.table, f.pages, tk, pos / kPageSize) * kPageSize + pos % kPageSize;
+        if (lane == 0) {
+            tok[t - t_lo] = make_int2(pos, slot);
+            if (e && reporter) atomicOr(p.err, e);
+        }
+    }
+}
+
+// Fused epilogue for this CTA's tokens of the tile (rows n0 + t): warp w takes
+// the range's tokens w, w + 4, ...; lane l sums features 4l..4l+3 of the token
 // over the NS partial tiles [token][feature] fp32 at the cluster addresses src
-// (NS = 1: this CTA's own tile, plain shared memory), rounds them to bf16 -- the
-// projection's output, as the pages' q/k/v tensors are bf16 -- and does the
-// segment's work: q -> norm + rope -> qhat; k -> norm + rope -> K[slot]; v -> V[slot].
+// (NS = 1: this CTA's own tile, plain shared memory), rounds them to bf16 --
+// the projection's output, as the pages' q/k/v tensors are bf16 -- and does
+// the segment's work: q -> norm + rope -> qhat; k -> norm + rope -> K[slot];
+// v -> V[slot].  The (position, slot) of each token come from fused_tokens; a
+// warp takes two tokens a pass and has all their loads in flight at once.
 template <int NS>
 __device__ __forceinline__ void fused_rows(const LinParams& p, const uint32_t (&src)[NS], const float* own,
-                                           int t_lo, int t_hi, int n0, int m0, int warp, int lane)
+                                           const int2* tok, int bn, int n0, int m0, int warp, int lane)
 {
     const LinFuse& f = p.f;
     const int seg = m0 < p.seg_end[0] ? 0 : (m0 < p.seg_end[1] ? 1 : 2);
@@ -100,67 +147,71 @@ __device__ __forceinline__ void fused_rows(const LinParams& p, const uint32_t (&
     const KRope kr = krope(lane, f.rot);
     float w4[4] = {0.f, 0.f, 0.f, 0.f};
     if (seg < 2) unpack4(reinterpret_cast<const uint2*>(seg == 0 ? f.qw : f.kw)[lane], w4);
-    for (int t = t_lo + warp; t < t_hi; t += 4) {
-        const int tok = n0 + t;
-        if (tok >= p.tokens) break;  // the same for the whole warp
-        const int pos = f.positions[tok];
-        float4 a;
+    int t_lo, t_hi;
+    fused_token_range(p, bn, t_lo, t_hi);
+    // (cos, sin) hi (and lo, for k) of this lane's table entries at a token's position
+    auto rope_rows = [&](int pos, float2 (&rh)[4], float2 (&rl)[4]) {
+        if (pos < 0 || seg == 2) return;
+        const float4* h4 = reinterpret_cast<const float4*>(f.rope_hi + (int64_t)pos * kRopeHalf + kr.f0);
+        const float4 h0 = h4[0], h1 = h4[1];
+        rh[0] = make_float2(h0.x, h0.y), rh[1] = make_float2(h0.z, h0.w), rh[2] = make_float2(h1.x, h1.y),
+        rh[3] = make_float2(h1.z, h1.w);
+        if (seg == 1) {
+            const float4* l4 = reinterpret_cast<const float4*>(f.rope_lo + (int64_t)pos * kRopeHalf + kr.f0);
+            const float4 l0 = l4[0], l1 = l4[1];
+            rl[0] = make_float2(l0.x, l0.y), rl[1] = make_float2(l0.z, l0.w), rl[2] = make_float2(l1.x, l1.y),
+            rl[3] = make_float2(l1.z, l1.w);
+        }
+    };
+    // the projected values of token t (features 4l..4l+3), summed over the NS partial tiles
+    auto partial = [&](int t, float4 (&v)[NS]) {
         if (NS == 1) {
-            a = reinterpret_cast<const float4*>(own)[t * (kBM / 4) + lane];
+            v[0] = reinterpret_cast<const float4*>(own)[t * (kBM / 4) + lane];
         } else {
-            float4 v[NS];
 #pragma unroll
             for (int q = 0; q < NS; ++q) v[q] = ld_cluster_f32x4(src[q] + (uint32_t)(t * kBM + 4 * lane) * 4);
-            a = v[0];
+        }
+    };
+    auto finish = [&](int t, const int2 cur, const float4 (&v)[NS], const float2 (&rh)[4], const float2 (&rl)[4]) {
+        float4 a = v[0];
 #pragma unroll
-            for (int q = 1; q < NS; ++q) {
-                a.x += v[q].x;
-                a.y += v[q].y;
-                a.z += v[q].z;
-                a.w += v[q].w;
-            }
+        for (int q = 1; q < NS; ++q) {
+            a.x += v[q].x;
+            a.y += v[q].y;
+            a.z += v[q].z;
+            a.w += v[q].w;
         }
         uint2 raw;
         raw.x = pack_bf16(__float2bfloat16_rn(a.x), __float2bfloat16_rn(a.y));
         raw.y = pack_bf16(__float2bfloat16_rn(a.z), __float2bfloat16_rn(a.w));
-        // the rows the attention would skip: position -1 (no step), out of range, or a page it cannot read
-        uint32_t e = 0;
-        if (pos != -1 && (pos < 0 || pos >= f.max_seq || pos >= f.pages * kPageSize)) e = PKV_DEVERR_POSITION;
-        int bad = 0;
-        if (pos >= 0 && !e)
-            for (int j = lane; j <= pos / kPageSize; j += 32) {
-                const int id = page_of(f.table, f.pages, tok, j);
-                bad |= (id < 0 || id >= f.num_pages);
-            }
-        if (__any_sync(kFull, bad)) e = PKV_DEVERR_PAGE;
-        if (pos == -1 || e) {
-            if (e && seg == 1 && head == 0 && lane == 0) atomicOr(p.err, e);
-            continue;
-        }
-        const int rf0 = kr.f0;
-        float2 rh[4], rl[4];
-        {
-            const float4* h4 = reinterpret_cast<const float4*>(f.rope_hi + (int64_t)pos * kRopeHalf + rf0);
-            const float4 h0 = h4[0], h1 = h4[1];
-            rh[0] = make_float2(h0.x, h0.y), rh[1] = make_float2(h0.z, h0.w), rh[2] = make_float2(h1.x, h1.y),
-            rh[3] = make_float2(h1.z, h1.w);
-        }
+        const int tk = n0 + t;
         if (seg == 0) {
-            *reinterpret_cast<float4*>(f.qhat + ((int64_t)tok * f.heads + head) * kHeadDim + 4 * lane) =
+            *reinterpret_cast<float4*>(f.qhat + ((int64_t)tk * f.heads + head) * kHeadDim + 4 * lane) =
                 norm_rope_q_regs(raw, w4, rh, f.eps, lane, f.rot);
-            continue;
-        }
-        const int64_t slot = (int64_t)page_of(f.table, f.pages, tok, pos / kPageSize) * kPageSize + pos % kPageSize;
-        const int64_t dst = ((int64_t)head * f.num_slots + slot) * kHeadDim + 4 * lane;
-        if (seg == 1) {
-            const float4* l4 = reinterpret_cast<const float4*>(f.rope_lo + (int64_t)pos * kRopeHalf + rf0);
-            const float4 l0 = l4[0], l1 = l4[1];
-            rl[0] = make_float2(l0.x, l0.y), rl[1] = make_float2(l0.z, l0.w), rl[2] = make_float2(l1.x, l1.y),
-            rl[3] = make_float2(l1.z, l1.w);
-            *reinterpret_cast<uint2*>(f.K + dst) = norm_rope_k_regs(raw, w4, rh, rl, f.eps, lane, f.rot);
         } else {
-            *reinterpret_cast<uint2*>(f.V + dst) = raw;  // v is written as given
+            const int64_t dst = ((int64_t)head * f.num_slots + cur.y) * kHeadDim + 4 * lane;
+            if (seg == 1)
+                *reinterpret_cast<uint2*>(f.K + dst) = norm_rope_k_regs(raw, w4, rh, rl, f.eps, lane, f.rot);
+            else
+                *reinterpret_cast<uint2*>(f.V + dst) = raw;  // v is written as given
         }
+    };
+    // two tokens a pass (t and t + 4): every load of both is in flight before the first is finished
+    for (int t = t_lo + warp; t < t_hi; t += 8) {
+        const int t2 = t + 4;
+        const int2 c0 = tok[t - t_lo], c1 = t2 < t_hi ? tok[t2 - t_lo] : make_int2(-1, 0);
+        float4 v0[NS], v1[NS];
+        float2 h0[4], l0[4], h1[4], l1[4];
+        if (c0.x >= 0) {
+            partial(t, v0);
+            rope_rows(c0.x, h0, l0);
+        }
+        if (c1.x >= 0) {
+            partial(t2, v1);
+            rope_rows(c1.x, h1, l1);
+        }
+        if (c0.x >= 0) finish(t, c0, v0, h0, l0);
+        if (c1.x >= 0) finish(t2, c1, v1, h1, l1);
     }
 }
 
@@ -279,6 +330,9 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
             tma_load_2d(a, &tmW, k * kBK, m0, fb, pol_w);
             tma_load_2d(a + S::kABytes, &tmX, k * kBK, n0, fb, pol_x);
         }
+    } else if (p.fused && warp >= 2) {
+        // ---- the fused epilogue's token table (positions, validity, slots), while the product runs
+        fused_tokens(p, reinterpret_cast<int2*>(sbase + S::kTok), BN, n0, m0, warp - 2, lane);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         constexpr uint32_t idesc = umma_idesc_bf16(kBM, BN, 0, 0);
@@ -326,7 +380,7 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
         }
         if (ok) {
             const uint32_t none[1] = {0u};
-            fused_rows<1>(p, none, part, 0, BN, n0, m0, warp, lane);
+            fused_rows<1>(p, none, part, reinterpret_cast<const int2*>(sbase + S::kTok), BN, n0, m0, warp, lane);
         }
         return;
     }
@@ -376,7 +430,7 @@ __global__ void __launch_bounds__(kLinThreads, BN == 64 ? 2 : 1)
             uint32_t src[NS];
 #pragma unroll
             for (int q = 0; q < NS; ++q) src[q] = cluster_map(local, q);
-            fused_rows<NS>(p, src, part, r * BN / NS, (r + 1) * BN / NS, n0, m0, warp, lane);
+            fused_rows<NS>(p, src, part, reinterpret_cast<const int2*>(sbase + S::kTok), BN, n0, m0, warp, lane);
         };
         switch (p.splits) {
         case 2: run(std::integral_constant<int, 2>{}); break;
@@ -405,7 +459,7 @@ cudaError_t launch_linear_bn(pkv_pool* pool, const void* x, const void* w, const
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(linear_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
     if (e != cudaSuccess) return e;
-    const bool timed = pool->timer_on;
+    const bool timed = pool->timer_on == 1;
     const int slot = timed ? (int)(pool->timer_count.fetch_add(1) % kTimerSlots) : 0;
     if (timed && (e = cudaEventRecord(pool->ev_start[slot], s)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
