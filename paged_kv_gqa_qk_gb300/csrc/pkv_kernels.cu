@@ -350,9 +350,12 @@ struct AttnSmem {
 // streaming rates differ by some 10-20% (the same pages take longer on some
 // SMs), so equal static slices alone end at different times; the chunks let
 // the fast CTAs take over the rest.  Q is 4 pages, or more where that keeps
-// ND <= kDynChunksPerCta * Ce (the partial slots of the workspace).
+// ND <= kDynChunksPerCta * Ce (the partial slots of the workspace).  (Smaller
+// chunks cost more than they balance: each is a segment of its own, with the
+// q preparation at its start and the merge and partial write at its end.)
 constexpr int kDynMinPagesPerCta = 8;
 constexpr int kDynChunkPages = 4;
+constexpr int kClaimAhead = 2;  // pages of a range still to issue when the next chunk is claimed
 
 struct Split {
     int64_t S;  // pages in static slices
@@ -571,12 +574,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         // Pages are read once, except the pages several rows share (a shared prompt
         // prefix): those stay in L2 for the other rows' reads, the rest go first.
         const uint64_t pol = l2_policy_evict_first(), pol_shared = l2_policy_evict_last();
-        // the static slice, then one claimed chunk after another; each claim is
-        // made when the range before it starts, so its answer is there at the end
+        // the static slice, then one claimed chunk after another.  A chunk is
+        // claimed when the range before it has kClaimAhead pages left to issue:
+        // late enough that the CTAs finishing first take the chunks, early enough
+        // that the counter's answer is there when the range ends.
         int64_t xb = (int64_t)c * sp.S / sp.Ce, xe = (int64_t)(c + 1) * sp.S / sp.Ce;
         int iv = c;  // the range's interval: partials of its pieces go to u + iv
         uint32_t claim = 0;
-        if (sp.ND && lane == 0) claim = atomicAdd(p.claim, 1u);
+        bool want = sp.ND > 0;  // the next chunk is still to be claimed
         for (;;) {
             int t, pre;
             find_token(p, sT0, sP0, xb, lane, t, pre);
@@ -609,6 +614,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                 const int seg_flags = (valid ? kFlagValid : 0) | ((j == 0 && has_last) ? kFlagComplete : 0);
                 for (int s = 0; s < seg; ++s, ++i) {
                     const int jj = j + s, st = i % kStages;
+                    if (want && xe - (x + s) <= kClaimAhead) {
+                        if (lane == 0) claim = atomicAdd(p.claim, 1u);
+                        want = false;
+                    }
                     if (i >= kStages &&
                         __any_sync(kFull, !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1, p.wait_ns) ||
                                               *abort_flag)) {
@@ -667,9 +676,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                 }
             }
             if (!ok || !sp.ND) break;
+            if (want && lane == 0) claim = atomicAdd(p.claim, 1u);  // (a range that issued nothing)
+            want = true;
             const uint32_t k = __shfl_sync(kFull, claim, 0);
             if (k >= (uint32_t)sp.ND) break;
-            if (lane == 0) claim = atomicAdd(p.claim, 1u);
             xb = sp.S + (int64_t)k * sp.Q;
             xe = xb + sp.Q;
             iv = sp.Ce + (int)k;
