@@ -485,6 +485,7 @@ def run_gpu(args) -> None:
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "sustained": sustained,
+        "gpu": torch.cuda.get_device_name(dev),
     }
     if wl.kind == "step":
         res["prompt_tokens_per_s"] = P * world / (ms_step / 1e3)
@@ -631,6 +632,7 @@ def run_gpu_linear(args) -> None:
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
     }
     pool.close()
     if rank == 0:
@@ -774,6 +776,7 @@ def run_gpu_layer(args) -> None:
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
         "sustained": sustained,
+        "gpu": torch.cuda.get_device_name(dev),
     }
     pool.close()
     if rank == 0:
