@@ -307,6 +307,7 @@ struct AttnParams {
     int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode, rot;
     int rows;                 // table rows (for the neighbouring-row comparison of shared pages)
     int prepared;             // decode mode with q prepared and k/v appended beforehand (pkv_decode_appended)
+    int late_wait;            // step mode after the prompt attention: see the launch wait in attn_kernel
     int64_t num_slots;
     float eps;
     uint64_t wait_ns;         // limit of the ring and group waits (the final drain always allows kWaitLimitNs)
@@ -520,8 +521,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     pdl_launch_dependents();
     __syncthreads();
     // Everything below reads the call's inputs and the pool, which the kernel
-    // before this one on the stream may have written.
-    pdl_wait();
+    // before this one on the stream may have written.  In step mode that kernel
+    // is the prompt attention, which writes nothing read here (only the prompt
+    // rows of the output) and releases this grid once it has itself waited for
+    // prep_kernel, whose writes this kernel reads: so this kernel starts on the
+    // SMs the prompt attention leaves, and waits for it only before it exits,
+    // which keeps the stream's completion order.
+    if (!p.late_wait) pdl_wait();
 
     // the norm weights, read once here (under the kernel's own streaming a
     // global load can wait microseconds)
@@ -565,7 +571,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     __syncthreads();
     const int64_t T = (int64_t)G * total;
     const Split sp = split_of(T, C);  // never more slices than pages: none is empty
-    if (c >= sp.Ce) return;
+    if (c >= sp.Ce) {
+        if (p.late_wait) pdl_wait();
+        return;
+    }
 
     if (warp == kProducerWarp) {
         // ================================================================ producer
@@ -996,6 +1005,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int k2 = max(0, n - kStages + (*s_stop_sent ? 1 : 0)); k2 < n; ++k2)
             mbar_wait(bar_full + 8 * (k2 % kStages), (k2 / kStages) & 1, kWaitLimitNs);
     }
+    if (p.late_wait) pdl_wait();
 }
 
 constexpr int kAttnStages = 3;
@@ -1049,6 +1059,7 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.decode_mode = decode_mode ? 1 : 0;
     p.qhat = a.q_hat;
     p.prepared = a.q_hat ? 1 : 0;
+    p.late_wait = (!decode_mode && pdl) ? 1 : 0;
     p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.num_slots = pool->num_slots;
     p.eps = static_cast<float>(pool->cfg.eps);

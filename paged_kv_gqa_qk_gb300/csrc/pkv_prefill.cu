@@ -737,6 +737,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tma_prefetch_desc(&tmV);
     }
     pdl_wait();  // prep_kernel's appends, token table and zeroed unit counter
+    // The kernel after this one in a step (the step rows' attention) reads only
+    // what prep_kernel wrote: it may start on the SMs this grid leaves, and
+    // waits for this grid before it ends.
+    pdl_launch_dependents();
 
     // ---- work items: the runs of every tile (a tile with none is one empty item,
     // so that its skipped tokens still get their zero output), in decreasing order
