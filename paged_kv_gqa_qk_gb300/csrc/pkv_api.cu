@@ -29,7 +29,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // unit split between intervals of the attention's work split: unit u's piece in
 // interval i sits at u + i, and there are at most C static slices plus
 // kDynChunksPerCta * C chunks, so U + C (1 + kDynChunksPerCta) slots.
-Plan make_plan(const pkv_pool* pool, int tokens, int pages)
+Plan make_plan(const pkv_pool* pool, int tokens, int pages, int prompt_tokens)
 {
     Plan pl;
     pl.tokens = tokens;
@@ -53,6 +53,8 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages)
     off = align_up(off + sizeof(float) * slots * kGroup, 256);
     pl.off_sched = off;
     off = align_up(off + sizeof(int32_t), 256);
+    pl.off_qhat = off;
+    off = align_up(off + (size_t)prompt_tokens * pool->cfg.heads * kHeadDim * 2, 256);
     pl.total = off;
     pl.claim = nullptr;
     return pl;
@@ -145,6 +147,20 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_heads(CUtensorMap* map, const void* base, int heads, int tokens)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, 32};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -357,7 +373,7 @@ static int run_step(pkv_pool* pool, const StepArgs& a, size_t ws_bytes, void* st
         const int rc = host_precheck(pool, a, static_cast<cudaStream_t>(stream));
         if (rc != PKV_OK) return rc;
     }
-    const Plan plan = make_plan(pool, a.P + a.steps, a.pages);
+    const Plan plan = make_plan(pool, a.P + a.steps, a.pages, a.P);
     if (!a.ws || ws_bytes < plan.total) return PKV_EWORKSPACE;
     return enqueue(pool, a, plan, static_cast<cudaStream_t>(stream));
 }
@@ -449,7 +465,7 @@ int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_t
     if (!pool || !bytes || rows < 0 || prefill_tokens < 0 || rows + prefill_tokens <= 0 || pages <= 0)
         return PKV_EINVAL;
     if ((int64_t)rows + prefill_tokens > (1 << 20) || (int64_t)rows * pages > INT32_MAX) return PKV_ERANGE;
-    *bytes = make_plan(pool, rows + prefill_tokens, pages).total;
+    *bytes = make_plan(pool, rows + prefill_tokens, pages, prefill_tokens).total;
     return PKV_OK;
 }
 
@@ -508,7 +524,7 @@ int pkv_decode_appended(pkv_pool* pool, const float* q_hat, const int32_t* posit
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;
     if (!table && (int64_t)rows * pages > pool->num_pages) return PKV_ERANGE;
-    const Plan plan = make_plan(pool, rows, pages);
+    const Plan plan = make_plan(pool, rows, pages, 0);
     if (!workspace || workspace_bytes < plan.total) return PKV_EWORKSPACE;
     const StepArgs a = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, positions, table,
                         0, rows, pages, rows, out, static_cast<char*>(workspace), q_hat};

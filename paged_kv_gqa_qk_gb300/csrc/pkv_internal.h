@@ -21,6 +21,9 @@ constexpr int kPageSize = 64;
 constexpr int kGroup = 4;                                  // query heads per kv head
 constexpr int kPageBytes = kPageSize * kHeadDim * 2;       // one page of K (or V) for one kv head
 constexpr int kRopeHalf = kHeadDim / 2;
+// The score scale the prompt attention's queries carry: log2(e) / sqrt(128), so that
+// its scores are in base-2 units.
+constexpr float kQScale = 1.4426950408889634f * 0.088388347648318440f;
 
 constexpr int kTimerSlots = 4096;
 
@@ -68,11 +71,12 @@ struct Plan {
     int ctas;           // attention grid size C
     size_t off_len, off_row, off_prefix, off_unit_ok, off_po, off_plse;
     size_t off_sched;   // prompt attention: counter of claimed work units (zeroed by prep_kernel)
+    size_t off_qhat;    // prompt tokens' queries after QK-norm, RoPE and kQScale: bf16 [P][heads][128]
     uint32_t* claim;    // decode attention: this call's chunk counter (reset by combine_kernel)
     size_t total;
 };
 
-Plan make_plan(const pkv_pool* pool, int tokens, int pages);
+Plan make_plan(const pkv_pool* pool, int tokens, int pages, int prompt_tokens);
 
 // Arguments of one decode/step call after host validation.
 struct StepArgs {
@@ -114,6 +118,10 @@ __device__ __forceinline__ int page_of(const int32_t* table, int pages, int row,
 // past the edges); false if the driver refuses it.
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                   uint32_t box_inner, uint32_t box_outer);
+// 3-D tiled tensor map {128 dims, heads, tokens} of bf16 [tokens][heads][128]; a box
+// is 64 dims (the 128-byte swizzle span) x 1 head x 32 tokens, zero fill past the
+// last token.
+bool make_tmap_heads(CUtensorMap* map, const void* base, int heads, int tokens);
 
 // y = x W^T (pkv_linear): tokens per tile, input-feature splits (CTAs of one
 // cluster), and the launch.

@@ -31,34 +31,39 @@
 namespace pkv {
 
 // =====================================================================================
-// prep_kernel (step mode): validate every token, append every token's k and v
+// prep_kernel (step mode): validate every token, append every token's k and v,
+// prepare the prompt tokens' queries
 // =====================================================================================
 struct PrepParams {
+    const __nv_bfloat16* q;
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
+    const __nv_bfloat16* qw;
     const __nv_bfloat16* kw;
     const int32_t* positions;       // [P]
     const int32_t* prow;            // [P]
     const int32_t* slots;           // [P] or null
     const int32_t* step_positions;  // [rows]
     const int32_t* table;           // [rows][pages], or null: contiguous rows
-    int P, rows, pages, num_pages, max_seq, kv_heads, rot;
+    int P, rows, pages, num_pages, max_seq, heads, kv_heads, rot;
     int64_t num_slots;
     float eps;
     const float2* rope_hi;          // (cos, sin) [max_seq][64], fp32 nearest to the double values
     const float2* rope_lo;          // the double values minus rope_hi, in fp32
     __nv_bfloat16* K;               // [kv_heads][num_slots][128]
     __nv_bfloat16* V;
+    __nv_bfloat16* q_hat;           // [P][heads][128]: the prompt attention's queries
     int32_t* tok_len;               // [tokens]  attended length, 0 = skip
     int32_t* tok_row;               // [tokens]  table row
     int32_t* sched;                 // work-unit counter of the prompt attention, zeroed here
     uint32_t* err;
 };
 
-// One CTA (4 warps) per token; warp w appends kv heads w, w+4, ...  Every
-// load that does not depend on another (the table entries, the slot, the
-// token's k and v, the RoPE row, the weights) is issued before the first use,
-// so that the token costs about two memory latencies.
+// One CTA (4 warps) per token; warp w appends kv heads w, w+4, ... and, for a
+// prompt token, prepares its query heads w, w+4, ...  Every load that does not
+// depend on another (the table entries, the slot, the token's q, k and v, the
+// RoPE row, the weights) is issued before the first use, so that the token
+// costs about two memory latencies.
 __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
 {
     const int t = blockIdx.x;
@@ -121,6 +126,18 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
     }
     float wk[4];
     unpack4(*reinterpret_cast<const uint2*>(p.kw + 4 * lane), wk);
+    // a prompt token's first query heads of this warp, and the q weights
+    constexpr int kQPre = 8;
+    const bool prompt = t < p.P;
+    uint2 qraw[kQPre] = {};
+    float wq[4] = {};
+    if (prompt) {
+#pragma unroll
+        for (int i = 0; i < kQPre; ++i)
+            if (warp + 4 * i < p.heads)
+                qraw[i] = *reinterpret_cast<const uint2*>(p.q + ((int64_t)t * p.heads + warp + 4 * i) * kHeadDim + 4 * lane);
+        unpack4(*reinterpret_cast<const uint2*>(p.qw + 4 * lane), wq);
+    }
 
     bad = __syncthreads_or(bad);
     if (inrange && bad) e = PKV_DEVERR_PAGE;
@@ -131,6 +148,25 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
         p.tok_len[t] = ok ? pos + 1 : 0;
         p.tok_row[t] = ok ? row : 0;
         if (e) atomicOr(p.err, e);
+    }
+    if (prompt) {
+        // the prompt attention's queries: QK-norm + RoPE (fp32 cos, sin), times
+        // kQScale, in bf16; zero for a skipped token
+        const bool ok = active && !e;
+        auto prep_q = [&](int hq, uint2 raw) {
+            uint2 r = make_uint2(0u, 0u);
+            if (ok) {
+                const float4 y = norm_rope_q_regs(raw, wq, rh, p.eps, lane, p.rot);
+                const float ys[4] = {y.x * kQScale, y.y * kQScale, y.z * kQScale, y.w * kQScale};
+                r = pack4(ys);
+            }
+            *reinterpret_cast<uint2*>(p.q_hat + ((int64_t)t * p.heads + hq) * kHeadDim + 4 * lane) = r;
+        };
+#pragma unroll
+        for (int i = 0; i < kQPre; ++i)
+            if (warp + 4 * i < p.heads) prep_q(warp + 4 * i, qraw[i]);
+        for (int hq = warp + 4 * kQPre; hq < p.heads; hq += 4)
+            prep_q(hq, *reinterpret_cast<const uint2*>(p.q + ((int64_t)t * p.heads + hq) * kHeadDim + 4 * lane));
     }
     if (!active || e) return;
 
@@ -153,8 +189,10 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
 cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
 {
     PrepParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.k = static_cast<const __nv_bfloat16*>(a.k);
     p.v = static_cast<const __nv_bfloat16*>(a.v);
+    p.qw = static_cast<const __nv_bfloat16*>(a.q_norm_w);
     p.kw = static_cast<const __nv_bfloat16*>(a.k_norm_w);
     p.positions = a.positions;
     p.prow = a.prow;
@@ -166,6 +204,7 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.pages = a.pages;
     p.num_pages = pool->num_pages;
     p.max_seq = pool->cfg.max_seq;
+    p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.num_slots = pool->num_slots;
@@ -174,6 +213,7 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.rope_lo = pool->rope_lo;
     p.K = static_cast<__nv_bfloat16*>(pool->k);
     p.V = static_cast<__nv_bfloat16*>(pool->v);
+    p.q_hat = reinterpret_cast<__nv_bfloat16*>(a.ws + plan.off_qhat);
     p.tok_len = reinterpret_cast<int32_t*>(a.ws + plan.off_len);
     p.tok_row = reinterpret_cast<int32_t*>(a.ws + plan.off_row);
     p.sched = reinterpret_cast<int32_t*>(a.ws + plan.off_sched);

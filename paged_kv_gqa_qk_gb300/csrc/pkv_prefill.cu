@@ -17,7 +17,10 @@
 //                            back into TMEM over the first half of S_h)
 //   O_h += P_h V_b           128 x 128, K = 128 keys   (tcgen05, A from TMEM)
 // Q carries the QK-norm, the RoPE and the score scale log2(e)/sqrt(128), so S
-// is in base-2 units.  The running max only moves (and O, l are rescaled in
+// is in base-2 units; prep_kernel prepares it once per token, and each unit
+// copies its 64 tokens x 4 heads into shared memory with the tensor-copy
+// engine (16 boxes of 32 tokens x 64 dims of one head, swizzled as the
+// products read them).  The running max only moves (and O, l are rescaled in
 // place) when a block raises it by more than 8: in between, P stays below 2^8.
 //
 // The two groups ping-pong: the tensor cores run one group's products while
@@ -26,10 +29,10 @@
 // so that S_h(b+1), which overwrites P_h(b) in tensor memory, is issued after
 // the product that reads it (tcgen05 operations of one thread run in order).
 //
-// Warp roles: 0-3 softmax group 0, 4-7 softmax group 1 (each also builds its
-// Q half and writes its outputs), 8 TMA producer (the K and the V of each
-// block through a ring of four 32 KiB stages), 9 tensor-memory allocation and
-// the MMA-issuing thread.
+// Warp roles: 0-3 softmax group 0, 4-7 softmax group 1 (each also writes its
+// outputs), 8 TMA producer (each unit's Q, then the K and the V of each block
+// through a ring of four 32 KiB stages), 9 tensor-memory allocation and the
+// MMA-issuing thread.
 //
 // The grid is persistent, one CTA per SM.  Units are taken from a counter in
 // the workspace in decreasing order of the tile's page count (longest first),
@@ -75,37 +78,25 @@ struct PfSmem {
     static constexpr int kSort = kRing + kPfStages * kPfStageBytes;  // uint32 [kMaxSortTiles]
     static constexpr int kTok = kSort + 4 * kMaxSortTiles;          // int pos[64], row[64]
     static constexpr int kRuns = kTok + 2 * kTileTok * 4;           // int row[64], npages[64], count, unit
-    static constexpr int kW = kRuns + (2 * kTileTok + 4) * 4;       // bf16 q_norm weights [128]
-    static constexpr int kBars = kW + 256;
-    // full[S], empty[S], s_ready[2], p_ready[2], o_done[2], epi[2], drain
-    static constexpr int kNumBars = 2 * kPfStages + 4 * kGroups + 1;
-    // at a unit's start the ring holds the tile's q rows and RoPE rows for the Q preparation
-    static constexpr int kStageQ = kRing;                           // [64 tokens][4 heads][128] bf16
-    static constexpr int kStageRope = kRing + kTileTok * kGroup * kHeadDim * 2;  // [64 tokens][64] float2
+    static constexpr int kBars = kRuns + (2 * kTileTok + 4) * 4;
+    // full[S], empty[S], s_ready[2], p_ready[2], o_done[2], epi[2], drain, q_full
+    static constexpr int kNumBars = 2 * kPfStages + 4 * kGroups + 2;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
     static constexpr int kFlag = kTmemSlot + 16;
     static constexpr int kBytes = kFlag + 16;
     static constexpr int kAlloc = kBytes + 1024;
 };
 static_assert(PfSmem::kAlloc <= 227 * 1024, "prefill shared memory");
-static_assert(PfSmem::kStageRope + kTileTok * kRopeHalf * 8 <= PfSmem::kRing + kPfStages * kPfStageBytes,
-              "staging fits the ring");
-
-// byte offset of element c (< 64) of row r in a [rows][64 bf16] tile with 128-byte swizzle
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2; }
+constexpr int kQBytes = kGroups * 2 * kRowsM * 128;  // a unit's Q: 64 tokens x 4 heads x 128 dims, bf16
 
 struct PfParams {
-    const __nv_bfloat16* q;   // [P + rows][heads][128], prompt tokens first
-    const __nv_bfloat16* qw;  // q_norm weights [128]
     const int32_t* tok_len;   // [P] attended length from prep_kernel, 0 = skip
     const int32_t* tok_row;   // [P]
     const int32_t* table;     // [rows][pages], or null (contiguous rows)
-    const float2* rope_hi;    // (cos, sin) [max_seq][64]
     __nv_bfloat16* out;       // [P + rows][heads][128]
     int32_t* sched;           // unit counter, zero at launch
     uint32_t* err;
-    int P, pages, heads, kv_heads, ntiles, rot;
-    float eps;
+    int P, pages, heads, kv_heads, ntiles;
 };
 
 
@@ -113,7 +104,7 @@ struct PfParams {
 struct PfCtx {
     uint32_t base;   // 1024-aligned shared address of the layout
     uint8_t* sbase;  // the same, generic
-    uint32_t bar_full, bar_empty, bar_s, bar_p, bar_o, bar_epi, bar_drain;
+    uint32_t bar_full, bar_empty, bar_s, bar_p, bar_o, bar_epi, bar_drain, bar_q;
     uint32_t tmem;
     int* sPos;
     int* sRow;
@@ -212,16 +203,30 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t vs, int h, int 
 
 // ---------------------------------------------------------------- producer (warp 8)
 __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p, const CUtensorMap* tmK,
-                                              const CUtensorMap* tmV, int lane)
+                                              const CUtensorMap* tmV, const CUtensorMap* tmQ, int lane)
 {
-    int q_load = 0;  // ring loads so far, across units
-    const uint64_t pol = l2_policy_evict_last();  // a prompt's tiles re-read the same pages
+    int q_load = 0;   // ring loads so far, across units
+    int q_units = 0;  // units whose Q has been requested
+    const uint64_t pol = l2_policy_evict_last();    // a prompt's tiles re-read the same pages
+    const uint64_t pol_q = l2_policy_evict_first();  // each unit's Q is read once
     for (;;) {
         if (lane == 0) *c.sUnit = atomicAdd(p.sched, 1);
         __syncthreads();  // (1)
         const int u = *c.sUnit;
         if (u >= c.nunits || *c.abort_flag) break;
         const int g = u % p.kv_heads;
+        if (lane == 0) {  // the unit's Q: the previous unit's products have all completed (barrier (4))
+            int tile, run;
+            item_of(c, p, u, tile, run);
+            mbar_arrive_expect_tx(c.bar_q, kQBytes);
+            for (int h = 0; h < kGroups; ++h)      // tokens 32h..32h+31 of the tile
+                for (int half = 0; half < 2; ++half)  // dims 64 half ..
+                    for (int j = 0; j < kGroup; ++j)  // query head g * 4 + j: rows 32j..32j+31
+                        tma_load_3d(c.base + PfSmem::kQ + h * (2 * kRowsM * 128) + half * (kRowsM * 128) +
+                                        j * (kHalfTok * 128),
+                                    tmQ, 64 * half, g * kGroup + j, tile * kTileTok + kHalfTok * h, c.bar_q, pol_q);
+        }
+        ++q_units;
         __syncthreads();  // (2)
         {  // the unit's runs: all of the tile's, or the one its item names
             int tile, run;
@@ -280,6 +285,8 @@ __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p,
         }
         __syncthreads();  // (4)
     }
+    // no copy in flight when the CTA ends (the issuer waited for every unit's Q unless it gave up)
+    if (lane == 0 && q_units > 0) mbar_wait(c.bar_q, (q_units - 1) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuer (warp 9, one thread)
@@ -288,6 +295,7 @@ __device__ __forceinline__ void issuer_role(const PfCtx& c, const PfParams& p, i
     const uint32_t qb = c.base + PfSmem::kQ, ring = c.base + PfSmem::kRing;
     const uint32_t tmem = c.tmem;
     int q_use = 0, it = 0, rc = 0;  // ring loads, blocks and runs so far, across units
+    int uq = 0;                     // units so far (one Q copy each)
     for (;;) {
         __syncthreads();  // (1)
         if (*c.sUnit >= c.nunits || *c.abort_flag) break;
@@ -297,7 +305,8 @@ __device__ __forceinline__ void issuer_role(const PfCtx& c, const PfParams& p, i
         tc_fence_after();
         const int nruns = *c.sNumRuns;
         if (lane == 0) {
-            bool ok = true;
+            bool ok = mbar_wait_spin(c.bar_q, uq & 1) && !*c.abort_flag;  // the unit's Q has landed
+            tc_fence_after();
             for (int r = 0; r < nruns && ok; ++r) {
                 const int n = c.sRunPages[r];
                 const int nb = (n + 1) / 2;
@@ -361,6 +370,7 @@ __device__ __forceinline__ void issuer_role(const PfCtx& c, const PfParams& p, i
         q_use = __shfl_sync(kAll, q_use, 0);
         it = __shfl_sync(kAll, it, 0);
         rc += nruns;
+        ++uq;
         tc_fence_before();
         __syncthreads();  // (4)
         tc_fence_after();
@@ -399,117 +409,7 @@ __device__ __forceinline__ void softmax_role(const PfCtx& c, const PfParams& p, 
         }
         __syncthreads();  // (2)
         const int pos = c.sPos[tok];
-        {  // stage the valid tokens' q rows (the 4 heads of g) and RoPE rows in the idle
-           // ring, coalesced: flat 16-byte chunk f of token f / 96 (64 chunks of q, 32 of
-           // RoPE).  Chunk w of token t sits at position w ^ (t % 8) of the token's row, so
-           // that both these writes and the per-row reads below are free of bank conflicts.
-            constexpr int kChunks = kTileTok * 96, kPer = kChunks / (32 * 4 * kGroups);
-            uint4 r[kPer];
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                const int f = tid + (32 * 4 * kGroups) * i, t = f / 96, w = f % 96;
-                const int tp = c.sPos[t];
-                r[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (tp >= 0)
-                    r[i] = w < 64 ? reinterpret_cast<const uint4*>(
-                                        p.q + ((int64_t)(p0 + t) * p.heads + g * kGroup) * kHeadDim)[w]
-                                  : reinterpret_cast<const uint4*>(p.rope_hi + (int64_t)tp * kRopeHalf)[w - 64];
-            }
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                const int f = tid + (32 * 4 * kGroups) * i, t = f / 96, w = f % 96;
-                const int off = w < 64 ? PfSmem::kStageQ + t * 1024 + 16 * (w ^ (t & 7))
-                                       : PfSmem::kStageRope + t * 512 + 16 * ((w - 64) ^ (t & 7));
-                *reinterpret_cast<uint4*>(c.sbase + off) = r[i];
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * 4 * kGroups) : "memory");  // the softmax warps only
-        }
         const int64_t qrow = ((int64_t)(p0 + tok) * p.heads + g * kGroup + wq) * kHeadDim;
-
-        // ---- Q: QK-norm + RoPE of this row, scaled by log2(e)/sqrt(128), bf16, swizzled
-        {
-            const int m = tid & (kRowsM - 1);
-            uint8_t* q0 = c.sbase + PfSmem::kQ + h * (2 * kRowsM * 128);
-            if (pos >= 0) {
-                // from the staged rows (chunk j of this row at position j ^ (tok % 8))
-                const uint8_t* qs = c.sbase + PfSmem::kStageQ + tok * (kGroup * kHeadDim * 2);
-                const uint8_t* rs = c.sbase + PfSmem::kStageRope + tok * (kRopeHalf * 8);
-                const int sw = tok & 7;
-                auto qchunk = [&](int k) {
-                    return *reinterpret_cast<const uint4*>(qs + 16 * ((wq * 16 + k) ^ sw));
-                };
-                const uint4* wsm = reinterpret_cast<const uint4*>(c.sbase + PfSmem::kW);
-                float ss = 0.f;
-#pragma unroll
-                for (int k = 0; k < kHeadDim / 8; ++k) {
-                    const uint4 r = qchunk(k);
-                    const uint32_t rv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float a = __uint_as_float(rv[e] << 16), b = __uint_as_float(rv[e] & 0xffff0000u);
-                        ss += a * a + b * b;
-                    }
-                }
-                const float inv =
-                    rsqrtf(ss * (1.0f / kHeadDim) + p.eps) * (1.4426950408889634f * 0.088388347648318440f);
-                // chunk c (dims 8c..8c+7) goes to Q half c / 8, chunk c % 8 of the row
-                auto store = [&](int c, const uint32_t (&w)[4]) {
-                    *reinterpret_cast<uint4*>(q0 + (c >> 3) * (kRowsM * 128) + sw128(m, 8 * (c & 7))) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                };
-                auto u_of = [](uint32_t x, uint32_t w, int b) {
-                    return __uint_as_float(b ? (x & 0xffff0000u) : (x << 16)) *
-                           __uint_as_float(b ? (w & 0xffff0000u) : (w << 16));
-                };
-                const int hc = p.rot / 16;  // chunks in a rotary half: chunk k pairs with k + hc
-#pragma unroll 4
-                for (int k = 0; k < hc; ++k) {  // dims 8k..8k+7 and their partners rot/2 further
-                    const uint4 rl = qchunk(k), rh = qchunk(k + hc);
-                    const uint4 wl = wsm[k], wh = wsm[k + hc];
-                    const uint32_t xl[4] = {rl.x, rl.y, rl.z, rl.w}, xh[4] = {rh.x, rh.y, rh.z, rh.w};
-                    const uint32_t vl[4] = {wl.x, wl.y, wl.z, wl.w}, vh[4] = {wh.x, wh.y, wh.z, wh.w};
-                    uint32_t lo[4], hi[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float y[2], z[2];
-                        const float4 cc =  // (cos, sin) of dims 8k + 2e and 8k + 2e + 1
-                            *reinterpret_cast<const float4*>(rs + 16 * ((4 * k + e) ^ sw));
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const float ul = u_of(xl[e], vl[e], b), uh = u_of(xh[e], vh[e], b);
-                            const float co = b ? cc.z : cc.x, si = b ? cc.w : cc.y;
-                            y[b] = inv * (ul * co - uh * si);  // y[d]         = u[d] cos - u[d+rot/2] sin
-                            z[b] = inv * (uh * co + ul * si);  // y[d + rot/2] = u[d+rot/2] cos + u[d] sin
-                        }
-                        const __nv_bfloat162 yl = __floats2bfloat162_rn(y[0], y[1]);
-                        const __nv_bfloat162 zh = __floats2bfloat162_rn(z[0], z[1]);
-                        lo[e] = *reinterpret_cast<const uint32_t*>(&yl);
-                        hi[e] = *reinterpret_cast<const uint32_t*>(&zh);
-                    }
-                    store(k, lo);
-                    store(k + hc, hi);
-                }
-                for (int c = 2 * hc; c < kHeadDim / 8; ++c) {  // dims RoPE leaves as they are
-                    const uint4 r = qchunk(c), w = wsm[c];
-                    const uint32_t x4[4] = {r.x, r.y, r.z, r.w}, w4[4] = {w.x, w.y, w.z, w.w};
-                    uint32_t o4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __nv_bfloat162 t = __floats2bfloat162_rn(inv * u_of(x4[e], w4[e], 0),
-                                                                       inv * u_of(x4[e], w4[e], 1));
-                        o4[e] = *reinterpret_cast<const uint32_t*>(&t);
-                    }
-                    store(c, o4);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    *reinterpret_cast<uint4*>(q0 + sw128(m, 8 * k)) = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(q0 + kRowsM * 128 + sw128(m, 8 * k)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q is read by the tensor cores
-        }
         tc_fence_before();
         __syncthreads();  // (3)
         tc_fence_after();
@@ -692,7 +592,8 @@ __device__ __forceinline__ void idle_role(const PfCtx& c)
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, PfParams p)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, PfParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -707,6 +608,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     c.bar_o = c.bar_p + 8 * kGroups;
     c.bar_epi = c.bar_o + 8 * kGroups;
     c.bar_drain = c.bar_epi + 8 * kGroups;
+    c.bar_q = c.bar_drain + 8;
     uint32_t* sKey = reinterpret_cast<uint32_t*>(c.sbase + PfSmem::kSort);
     c.sKey = sKey;
     c.sPos = reinterpret_cast<int*>(c.sbase + PfSmem::kTok);
@@ -728,6 +630,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(c.bar_epi + 8 * h, 4);
         }
         mbar_init(c.bar_drain, 1);
+        mbar_init(c.bar_q, 1);
         *c.abort_flag = 0;
         fence_mbar_init();
     }
@@ -735,6 +638,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp == kProducer && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmQ);
     }
     pdl_wait();  // prep_kernel's appends, token table and zeroed unit counter
     // The kernel after this one in a step (the step rows' attention) reads only
@@ -747,8 +651,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // of pages, ties in token order
     const int ntiles = p.ntiles;
     int* sNItems = c.sUnit + 1;
-    if (tid < kHeadDim / 4)
-        reinterpret_cast<uint2*>(c.sbase + PfSmem::kW)[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
     if (tid == 0) *sNItems = 0;
     __syncthreads();
     if (ntiles <= kMaxSortTiles) {
@@ -808,7 +710,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp >= kProducer) {
         regs_dec<kRegsOther>();
         if (warp == kProducer)
-            producer_role(c, p, &tmK, &tmV, lane);
+            producer_role(c, p, &tmK, &tmV, &tmQ, lane);
         else if (warp == kIssuer)
             issuer_role(c, p, lane);
         else
@@ -835,12 +737,9 @@ cudaError_t configure_prefill()
 cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, cudaStream_t s)
 {
     PfParams p;
-    p.q = static_cast<const __nv_bfloat16*>(a.q);
-    p.qw = static_cast<const __nv_bfloat16*>(a.q_norm_w);
     p.tok_len = reinterpret_cast<const int32_t*>(a.ws + plan.off_len);
     p.tok_row = reinterpret_cast<const int32_t*>(a.ws + plan.off_row);
     p.table = a.table;
-    p.rope_hi = pool->rope_hi;
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.sched = reinterpret_cast<int32_t*>(a.ws + plan.off_sched);
     p.err = pool->err;
@@ -849,8 +748,9 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.ntiles = (a.P + kTileTok - 1) / kTileTok;
-    p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
-    p.eps = static_cast<float>(pool->cfg.eps);
+    // the prompt tokens' queries prep_kernel prepared in the workspace
+    CUtensorMap tmQ;
+    if (!make_tmap_heads(&tmQ, a.ws + plan.off_qhat, p.heads, a.P)) return cudaErrorInvalidValue;
     const int units = p.ntiles * p.kv_heads;
     const int grid = ctas < units ? ctas : units;
     cudaLaunchConfig_t cfg = {};
@@ -863,7 +763,7 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel, pool->tmap_k, pool->tmap_v, p);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel, pool->tmap_k, pool->tmap_v, tmQ, p);
 }
 
 }  // namespace pkv

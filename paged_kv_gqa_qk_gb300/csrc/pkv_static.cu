@@ -60,7 +60,7 @@ extern "C" int pkv_decode_static(pkv_pool* pool, const void* q, const void* k, c
         !aligned_to(q_norm_w, 8) || !aligned_to(k_norm_w, 8) || !aligned_to(positions, 4) || !aligned_to(table, 4))
         return PKV_EINVAL;
     if (!table && (int64_t)rows * pages > pool->num_pages) return PKV_ERANGE;
-    const pkv::Plan plan = pkv::make_plan(pool, rows, pages);
+    const pkv::Plan plan = pkv::make_plan(pool, rows, pages, 0);
     if (plan.total > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERANGE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pool->device) return PKV_EDEVICE;

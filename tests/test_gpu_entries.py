@@ -46,6 +46,30 @@ def test_prefill_2048_tokens():
     compare(wl, run_gpu(wl), run_oracle(wl), label="prefill P=2048 (all tokens)")
 
 
+def _tile_items(lengths) -> int:
+    """(64-token tile, prompt) pairs of prompts packed end to end: the prompt
+    attention's work items."""
+    items, t0 = 0, 0
+    ends = np.cumsum(lengths)
+    starts = ends - np.asarray(lengths)
+    for t0 in range(0, int(ends[-1]), 64):
+        items += int(((starts < t0 + 64) & (ends > t0)).sum())
+    return items
+
+
+@pytest.mark.parametrize("prompt_len,prompts,sorted_items", [(40, 150, True), (2, 2400, False)])
+def test_prefill_many_short_prompts(prompt_len, prompts, sorted_items):
+    """Many short prompts, several to a 64-token tile.  Up to 2048 work items
+    (one per prompt in a tile) go longest first; more than that, and the tiles
+    go in token order with all their prompts in one unit."""
+    gen = torch.Generator().manual_seed(37 + prompts)
+    lens = torch.randint(1, prompt_len + 1, (prompts,), generator=gen).tolist()
+    starts = torch.randint(0, 301, (prompts,), generator=gen).tolist()
+    assert (_tile_items(lens) <= 2048) == sorted_items
+    wl = W.make_prefill(f"prefill {prompts} short prompts", lens, starts, seed=37, table_pages=6, gen=gen)
+    compare(wl, run_gpu(wl), run_oracle(wl), label=f"prefill {prompts} short prompts")
+
+
 def test_prefill_invalid_tokens():
     wl = W.make_prefill("prefill errors", [40, 30, 20], [0, 100, 5], seed=33, table_pages=4)
     pos = wl.positions.clone()
