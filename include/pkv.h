@@ -168,7 +168,9 @@ PKV_API int pkv_pool_kv(const pkv_pool* pool, void** k, void** v, int64_t* num_s
  * initialisation and are not meaningful after the call.  The size depends
  * only on the pool (its config and attention grid size, see pkv_set_ctas),
  * rows and prefill_tokens: about 16.5 KiB per token plus 35 KiB per attention
- * CTA (room for the partial results of the pieces the work split makes).
+ * CTA (room for the partial results of the pieces the work split makes), and
+ * per prompt token heads * head_dim * 2 bytes more (8 KiB at the defaults) for
+ * its queries, prepared once before the prompt attention.
  * Errors: PKV_EINVAL (null, rows < 0, prefill_tokens < 0, both zero,
  * pages <= 0), PKV_ERANGE (more than 2^20 tokens). */
 PKV_API int pkv_workspace_bytes(const pkv_pool* pool, int rows, int pages, int prefill_tokens, size_t* bytes);
