@@ -203,14 +203,17 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t vs, int h, int 
 
 // ---------------------------------------------------------------- producer (warp 8)
 __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p, const CUtensorMap* tmK,
-                                              const CUtensorMap* tmV, const CUtensorMap* tmQ, int lane)
+                                              const CUtensorMap* tmV, const CUtensorMap* tmQ, int first_claim,
+                                              int lane)
 {
     int q_load = 0;   // ring loads so far, across units
     int q_units = 0;  // units whose Q has been requested
     const uint64_t pol = l2_policy_evict_last();    // a prompt's tiles re-read the same pages
     const uint64_t pol_q = l2_policy_evict_first();  // each unit's Q is read once
+    bool first = true;
     for (;;) {
-        if (lane == 0) *c.sUnit = atomicAdd(p.sched, 1);
+        if (lane == 0) *c.sUnit = first ? first_claim : atomicAdd(p.sched, 1);
+        first = false;
         __syncthreads();  // (1)
         const int u = *c.sUnit;
         if (u >= c.nunits || *c.abort_flag) break;
@@ -645,6 +648,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // what prep_kernel wrote: it may start on the SMs this grid leaves, and
     // waits for this grid before it ends.
     pdl_launch_dependents();
+    // the producer's first unit is claimed now; the answer is needed after the sort
+    int first_claim = 0;
+    if (warp == kProducer && lane == 0) first_claim = atomicAdd(p.sched, 1);
 
     // ---- work items: the runs of every tile (a tile with none is one empty item,
     // so that its skipped tokens still get their zero output), in decreasing order
@@ -654,14 +660,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (tid == 0) *sNItems = 0;
     __syncthreads();
     if (ntiles <= kMaxSortTiles) {
-        for (int t = warp; t < ntiles; t += kPfThreads / 32) {
+        // warp w takes tiles w, w + 12, ...: the lengths and rows of kScanBatch of
+        // them are loaded before the first is looked at (one memory latency a batch)
+        constexpr int kWarps = kPfThreads / 32, kScanBatch = 4;
+        for (int t0 = warp; t0 < ntiles; t0 += kScanBatch * kWarps) {
+            int lens[kScanBatch][2], rows[kScanBatch][2];
+#pragma unroll
+            for (int bt = 0; bt < kScanBatch; ++bt)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int tok = (t0 + bt * kWarps) * kTileTok + lane + 32 * i;
+                    const bool in = t0 + bt * kWarps < ntiles && tok < p.P;
+                    lens[bt][i] = in ? p.tok_len[tok] : 0;
+                    rows[bt][i] = in ? p.tok_row[tok] : -1;
+                }
+#pragma unroll
+            for (int bt = 0; bt < kScanBatch; ++bt) {
+            const int t = t0 + bt * kWarps;
+            if (t >= ntiles) break;  // the same for the whole warp
             int pos2[2], row2[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int tok = t * kTileTok + lane + 32 * i;
-                const int len = tok < p.P ? p.tok_len[tok] : 0;
-                pos2[i] = len - 1;
-                row2[i] = len > 0 ? p.tok_row[tok] : -1;
+                pos2[i] = lens[bt][i] - 1;
+                row2[i] = lens[bt][i] > 0 ? rows[bt][i] : -1;
             }
             auto add = [&](int run, int pages) {
                 if (lane == 0) {
@@ -673,6 +694,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             };
             const int nr = tile_runs(pos2[0], pos2[1], row2[0], row2[1], [&](int i, int, int pages) { add(i, pages); });
             if (nr == 0) add(0, 0);
+            }
         }
     } else if (tid == 0) {
         *sNItems = kMaxSortTiles + 1;
@@ -681,7 +703,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int nitems = *sNItems;
     c.sorted = nitems <= kMaxSortTiles;
     c.nunits = (c.sorted ? nitems : ntiles) * p.kv_heads;
-    if (c.sorted) {
+    if (c.sorted && nitems <= kPfThreads) {
+        // one key a thread; keys are distinct (each names its tile and run), so a
+        // key's place in decreasing order is the number of larger keys
+        uint32_t key = 0;
+        int rank = 0;
+        if (tid < nitems) {
+            key = sKey[tid];
+            for (int i = 0; i < nitems; ++i) rank += sKey[i] > key;
+        }
+        __syncthreads();
+        if (tid < nitems) sKey[rank] = key;
+    } else if (c.sorted) {
         int n2 = 1;
         while (n2 < nitems) n2 <<= 1;
         for (int i = nitems + tid; i < n2; i += kPfThreads) sKey[i] = 0;
@@ -710,7 +743,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp >= kProducer) {
         regs_dec<kRegsOther>();
         if (warp == kProducer)
-            producer_role(c, p, &tmK, &tmV, &tmQ, lane);
+            producer_role(c, p, &tmK, &tmV, &tmQ, first_claim, lane);
         else if (warp == kIssuer)
             issuer_role(c, p, lane);
         else
