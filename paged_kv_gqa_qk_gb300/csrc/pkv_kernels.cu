@@ -34,6 +34,8 @@ namespace pkv {
 // prep_kernel (step mode): validate every token, append every token's k and v,
 // prepare the prompt tokens' queries
 // =====================================================================================
+constexpr int kPrepWarps = 4;                 // warps of a token's CTA
+constexpr int kKvPre = 8 / kPrepWarps;        // kv heads a warp loads before the first use (of 8)
 struct PrepParams {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -59,15 +61,42 @@ struct PrepParams {
     uint32_t* err;
 };
 
-// One CTA (4 warps) per token; warp w appends kv heads w, w+4, ... and, for a
-// prompt token, prepares its query heads w, w+4, ...  Every load that does not
-// depend on another (the table entries, the slot, the token's q, k and v, the
-// RoPE row, the weights) is issued before the first use, so that the token
-// costs about two memory latencies.
-__global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
+// One CTA (kPrepWarps warps) per token; warp w appends kv heads w, w + 4, ...
+// and, for a prompt token, prepares its query heads w, w + 4, ...  The loads
+// that depend only on the token index (its q, k and v) go out first, the ones
+// that need its row and position (the table entries, the slot, the RoPE row)
+// next, all before the first use, so that the token costs about two memory
+// latencies.  (Four warps a token measured faster than one, two or eight: the
+// per-warp chain of norms outweighs the residency fewer threads would give.)
+__global__ void __launch_bounds__(32 * kPrepWarps) prep_kernel(PrepParams p)
 {
     const int t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // first the loads that depend on nothing but t: the token's k and v for
+    // this warp's first kv heads, a prompt token's first query heads of this
+    // warp and the q weights
+    uint2 kraw[kKvPre] = {}, vraw[kKvPre] = {};
+#pragma unroll
+    for (int i = 0; i < kKvPre; ++i) {
+        const int g = warp + kPrepWarps * i;
+        if (g < p.kv_heads) {
+            const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim + 4 * lane;
+            kraw[i] = *reinterpret_cast<const uint2*>(p.k + src);
+            vraw[i] = *reinterpret_cast<const uint2*>(p.v + src);
+        }
+    }
+    constexpr int kQPre = 32 / kPrepWarps;
+    const bool prompt = t < p.P;
+    uint2 qraw[kQPre] = {};
+    float wq[4] = {};
+    if (prompt) {
+#pragma unroll
+        for (int i = 0; i < kQPre; ++i)
+            if (warp + kPrepWarps * i < p.heads)
+                qraw[i] = *reinterpret_cast<const uint2*>(p.q + ((int64_t)t * p.heads + warp + kPrepWarps * i) * kHeadDim + 4 * lane);
+        unpack4(*reinterpret_cast<const uint2*>(p.qw + 4 * lane), wq);
+    }
 
     int row, pos;
     bool active = true;
@@ -101,18 +130,8 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
         else
             slot = (int64_t)page_of(p.table, p.pages, row, pos / kPageSize) * kPageSize + pos % kPageSize;
     }
-    // the token's k and v for this warp's first two kv heads, its RoPE row, the weights
+    // the token's RoPE row and the k weights
     const int pc = inrange ? pos : 0;
-    uint2 kraw[2] = {}, vraw[2] = {};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int g = warp + 4 * i;
-        if (g < p.kv_heads) {
-            const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim + 4 * lane;
-            kraw[i] = *reinterpret_cast<const uint2*>(p.k + src);
-            vraw[i] = *reinterpret_cast<const uint2*>(p.v + src);
-        }
-    }
     float2 rh[4], rl[4];
     {
         const int f0 = krope(lane, p.rot).f0;
@@ -126,18 +145,6 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
     }
     float wk[4];
     unpack4(*reinterpret_cast<const uint2*>(p.kw + 4 * lane), wk);
-    // a prompt token's first query heads of this warp, and the q weights
-    constexpr int kQPre = 8;
-    const bool prompt = t < p.P;
-    uint2 qraw[kQPre] = {};
-    float wq[4] = {};
-    if (prompt) {
-#pragma unroll
-        for (int i = 0; i < kQPre; ++i)
-            if (warp + 4 * i < p.heads)
-                qraw[i] = *reinterpret_cast<const uint2*>(p.q + ((int64_t)t * p.heads + warp + 4 * i) * kHeadDim + 4 * lane);
-        unpack4(*reinterpret_cast<const uint2*>(p.qw + 4 * lane), wq);
-    }
 
     bad = __syncthreads_or(bad);
     if (inrange && bad) e = PKV_DEVERR_PAGE;
@@ -164,25 +171,23 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepParams p)
         };
 #pragma unroll
         for (int i = 0; i < kQPre; ++i)
-            if (warp + 4 * i < p.heads) prep_q(warp + 4 * i, qraw[i]);
-        for (int hq = warp + 4 * kQPre; hq < p.heads; hq += 4)
+            if (warp + kPrepWarps * i < p.heads) prep_q(warp + kPrepWarps * i, qraw[i]);
+        for (int hq = warp + kPrepWarps * kQPre; hq < p.heads; hq += kPrepWarps)
             prep_q(hq, *reinterpret_cast<const uint2*>(p.q + ((int64_t)t * p.heads + hq) * kHeadDim + 4 * lane));
     }
     if (!active || e) return;
 
-    for (int g = warp, i = 0; g < p.kv_heads; g += 4, ++i) {
+    auto append = [&](int g, uint2 kr, uint2 vr) {
         const int64_t dst = ((int64_t)g * p.num_slots + slot) * kHeadDim + 4 * lane;
-        uint2 kr, vr;
-        if (i < 2) {
-            kr = kraw[i & 1];
-            vr = vraw[i & 1];
-        } else {
-            const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim + 4 * lane;
-            kr = *reinterpret_cast<const uint2*>(p.k + src);
-            vr = *reinterpret_cast<const uint2*>(p.v + src);
-        }
         *reinterpret_cast<uint2*>(p.K + dst) = norm_rope_k_regs(kr, wk, rh, rl, p.eps, lane, p.rot);
         *reinterpret_cast<uint2*>(p.V + dst) = vr;  // v is written as given
+    };
+#pragma unroll
+    for (int i = 0; i < kKvPre; ++i)
+        if (warp + kPrepWarps * i < p.kv_heads) append(warp + kPrepWarps * i, kraw[i], vraw[i]);
+    for (int g = warp + kPrepWarps * kKvPre; g < p.kv_heads; g += kPrepWarps) {
+        const int64_t src = ((int64_t)t * p.kv_heads + g) * kHeadDim + 4 * lane;
+        append(g, *reinterpret_cast<const uint2*>(p.k + src), *reinterpret_cast<const uint2*>(p.v + src));
     }
 }
 
@@ -218,7 +223,7 @@ cudaError_t launch_prep(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.tok_row = reinterpret_cast<int32_t*>(a.ws + plan.off_row);
     p.sched = reinterpret_cast<int32_t*>(a.ws + plan.off_sched);
     p.err = pool->err;
-    prep_kernel<<<a.P + a.steps, 128, 0, s>>>(p);
+    prep_kernel<<<a.P + a.steps, 32 * kPrepWarps, 0, s>>>(p);
     return cudaGetLastError();
 }
 
