@@ -70,6 +70,20 @@ def test_prefill_many_short_prompts(prompt_len, prompts, sorted_items):
     compare(wl, run_gpu(wl), run_oracle(wl), label=f"prefill {prompts} short prompts")
 
 
+@pytest.mark.parametrize("kv_heads", [2, 16])
+def test_prompt_paths_other_head_counts(kv_heads):
+    """Prefill and step with 4 x kv_heads query heads other than Qwen3-8B's 32:
+    the prompt tokens' prepared queries (64 heads take the per-warp loop past
+    its first eight heads) and each unit's copy of its four heads' rows."""
+    cfg = dict(kv_heads=kv_heads, heads=4 * kv_heads)
+    wl = W.make_prefill(f"prefill {kv_heads} kv heads", [70, 130, 9], [60, 0, 200], seed=38, cfg=cfg,
+                        table_pages=5)
+    compare(wl, run_gpu(wl), run_oracle(wl), label=f"prefill, {kv_heads} kv heads")
+    wl = W.make_step(f"step {kv_heads} kv heads", [100, 40], [0, 300], [700, 64, 1, 333], seed=39, cfg=cfg,
+                     table_pages=12)
+    compare(wl, run_gpu(wl), run_oracle(wl), label=f"step, {kv_heads} kv heads")
+
+
 def test_prefill_invalid_tokens():
     wl = W.make_prefill("prefill errors", [40, 30, 20], [0, 100, 5], seed=33, table_pages=4)
     pos = wl.positions.clone()
