@@ -319,23 +319,27 @@ def run_gpu(args) -> None:
     out = torch.empty_like(q)
     ws = pool.workspace(0 if wl.kind == "prefill" else R, pages, P)
     stream = torch.cuda.Stream(device=dev)
-    if wl.kind == "decode":
-        def step():
-            pkv.pkv_decode(pool.handle, q, k, v, qw, kw, pos, tab, out, ws, stream, pages=pages)
-        launches_per_step = 2   # attention, combine
-    elif wl.kind == "step":  # step_paged: prompt chunks + one step per row
+    ppos = prow = None
+    if wl.kind != "decode":
         ppos, prow = wl.positions.to(dev), wl.prow.to(dev)
 
-        def step():
-            pkv.pkv_step(pool.handle, q, k, v, qw, kw, ppos, prow, None, pos, tab, out, ws, stream, pages=pages)
-        launches_per_step = 4   # prep, prompt attention, step-row attention, combine
-    else:  # prefill_paged: prompt chunks only
-        ppos, prow = wl.positions.to(dev), wl.prow.to(dev)
+    def make_step(b, o):
+        """One call of the library on buffer set b = (q, k, v, pos, tab, ppos, prow), writing o."""
+        bq, bk, bv, bpos, btab, bppos, bprow = b
+        if wl.kind == "decode":
+            return lambda: pkv.pkv_decode(pool.handle, bq, bk, bv, qw, kw, bpos, btab, o, ws, stream, pages=pages)
+        if wl.kind == "step":  # step_paged: prompt chunks + one step per row
+            return lambda: pkv.pkv_step(pool.handle, bq, bk, bv, qw, kw, bppos, bprow, None, bpos, btab, o, ws, stream,
+                                        pages=pages)
+        # prefill_paged: prompt chunks only
+        return lambda: pkv.pkv_prefill(pool.handle, bq, bk, bv, qw, kw, bppos, bprow, None, btab, o, ws, stream,
+                                       rows=R, pages=pages)
 
-        def step():
-            pkv.pkv_prefill(pool.handle, q, k, v, qw, kw, ppos, prow, None, tab, out, ws, stream, rows=R,
-                            pages=pages)
-        launches_per_step = 2   # prep, prompt attention
+    bufs = (q, k, v, pos, tab, ppos, prow)
+    step = make_step(bufs, out)
+    # decode: attention, combine; step: prep, prompt attention, step-row attention, combine;
+    # prefill: prep, prompt attention
+    launches_per_step = {"decode": 2, "step": 4}.get(wl.kind, 2)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -393,7 +397,9 @@ def run_gpu(args) -> None:
     ms_step = ms_total / args.steps
 
     # ---- end-to-end through the C ABI with host buffers: inputs H2D from pinned
-    # memory and the output D2H, every step, inside the timed region
+    # memory and the output D2H, every step, inside the timed region.  As a serving
+    # loop would, it keeps two device buffer sets: step i+1's inputs go up on one copy
+    # stream and step i's output comes back on another while step i runs.
     host_in = [t.pin_memory() for t in (host_q, host_k, host_v)]
     dev_in = [q, k, v]
     if wl.kind != "prefill":
@@ -405,20 +411,42 @@ def run_gpu(args) -> None:
     if wl.kind != "decode":
         host_in += [wl.positions.pin_memory(), wl.prow.pin_memory()]
         dev_in += [ppos, prow]
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host_out = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    dev_in2 = [d.clone() for d in dev_in]
+    clone_of = {id(d): d2 for d, d2 in zip(dev_in, dev_in2)}
+    out2 = torch.empty_like(out)
+    sets = [(dev_in, make_step(bufs, out), out),
+            (dev_in2, make_step(tuple(clone_of.get(id(t), t) for t in bufs), out2), out2)]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = {name: [torch.cuda.Event(), torch.cuda.Event()] for name in ("landed", "read", "written", "fetched")}
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            flush()
-            for d, h in zip(dev_in, host_in):
+    for i in range(args.steps):
+        j = i & 1
+        d_in, st, o = sets[j]
+        with torch.cuda.stream(up):      # step i's inputs, once step i-2 has read set j
+            if i >= 2:
+                up.wait_event(ev["read"][j])
+            for d, h in zip(d_in, host_in):
                 d.copy_(h, non_blocking=True)
-            step()
-            host_out.copy_(out, non_blocking=True)
-        stream.synchronize()
+            ev["landed"][j].record(up)
+        with torch.cuda.stream(stream):  # step i, once its inputs are in and step i-2's output is out
+            flush()
+            stream.wait_event(ev["landed"][j])
+            if i >= 2:
+                stream.wait_event(ev["fetched"][j])
+            st()
+            ev["read"][j].record(stream)
+            ev["written"][j].record(stream)
+        with torch.cuda.stream(down):    # step i's output
+            down.wait_event(ev["written"][j])
+            host_out[j].copy_(o, non_blocking=True)
+            ev["fetched"][j].record(down)
+    for st_ in (up, stream, down):
+        st_.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
     flags = pkv.pkv_check_errors(pool.handle, stream)
@@ -481,7 +509,9 @@ def run_gpu(args) -> None:
         "kv_gbs_unique": wl.meta.get("unique_kv_bytes", logical) / (ms_step / 1e3) / 1e9 * world,
         "roofline": roofline,
         "e2e": {"value": rows_total * args.steps / e2e_s, "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "copies": "every step's inputs H2D and output D2H; two device buffer sets, step i+1's inputs "
+                          "and step i's output copied on their own streams while step i runs"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "sustained": sustained,
