@@ -291,6 +291,49 @@ def sustained_pass(step, flush, stream, ms_step_hint: float, seconds: float, blo
 
 # ---------------------------------------------------------------------------- the GPU arm
 
+def double_buffered_e2e(steps: int, sets, host_in, flush, stream, dev) -> float:
+    """Wall-clock seconds of `steps` end-to-end steps.  sets[j] = (device inputs,
+    run, device outputs, host outputs) for j = 0, 1: step i uses set i % 2; its
+    inputs go up from the pinned host_in on one copy stream and its outputs come
+    back on another, while the step before or after it runs on `stream`
+    (event-fenced: a set's inputs are rewritten only after the step that read
+    them, its outputs only after they were copied back)."""
+    import torch
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    landed, done, fetched = ([torch.cuda.Event(), torch.cuda.Event()] for _ in range(3))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        j = i & 1
+        d_in, run, d_out, h_out = sets[j]
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(done[j])
+            for d, h in zip(d_in, host_in):
+                d.copy_(h, non_blocking=True)
+            landed[j].record(up)
+        with torch.cuda.stream(stream):
+            if flush is not None:
+                flush()
+            stream.wait_event(landed[j])
+            if i >= 2:
+                stream.wait_event(fetched[j])
+            run()
+            done[j].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(done[j])
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+            fetched[j].record(down)
+    for st in (up, stream, down):
+        st.synchronize()
+    return time.perf_counter() - t0
+
+
+E2E_COPIES = ("every step's inputs H2D and outputs D2H; two device buffer sets, step i+1's inputs and step i's "
+              "outputs copied on their own streams while step i runs")
+
+
 def run_gpu(args) -> None:
     import torch
     import paged_kv_gqa_qk_gb300 as pkv
@@ -417,37 +460,11 @@ def run_gpu(args) -> None:
     dev_in2 = [d.clone() for d in dev_in]
     clone_of = {id(d): d2 for d, d2 in zip(dev_in, dev_in2)}
     out2 = torch.empty_like(out)
-    sets = [(dev_in, make_step(bufs, out), out),
-            (dev_in2, make_step(tuple(clone_of.get(id(t), t) for t in bufs), out2), out2)]
-    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev = {name: [torch.cuda.Event(), torch.cuda.Event()] for name in ("landed", "read", "written", "fetched")}
+    sets = [(dev_in, make_step(bufs, out), [out], [host_out[0]]),
+            (dev_in2, make_step(tuple(clone_of.get(id(t), t) for t in bufs), out2), [out2], [host_out[1]])]
     barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        j = i & 1
-        d_in, st, o = sets[j]
-        with torch.cuda.stream(up):      # step i's inputs, once step i-2 has read set j
-            if i >= 2:
-                up.wait_event(ev["read"][j])
-            for d, h in zip(d_in, host_in):
-                d.copy_(h, non_blocking=True)
-            ev["landed"][j].record(up)
-        with torch.cuda.stream(stream):  # step i, once its inputs are in and step i-2's output is out
-            flush()
-            stream.wait_event(ev["landed"][j])
-            if i >= 2:
-                stream.wait_event(ev["fetched"][j])
-            st()
-            ev["read"][j].record(stream)
-            ev["written"][j].record(stream)
-        with torch.cuda.stream(down):    # step i's output
-            down.wait_event(ev["written"][j])
-            host_out[j].copy_(o, non_blocking=True)
-            ev["fetched"][j].record(down)
-    for st_ in (up, stream, down):
-        st_.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_s = double_buffered_e2e(args.steps, sets, host_in, flush, stream, dev)
+    e2e_s = max_over_ranks(e2e_s, world)
     barrier(world)
     flags = pkv.pkv_check_errors(pool.handle, stream)
     if flags:
@@ -510,8 +527,7 @@ def run_gpu(args) -> None:
         "roofline": roofline,
         "e2e": {"value": rows_total * args.steps / e2e_s, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "copies": "every step's inputs H2D and output D2H; two device buffer sets, step i+1's inputs "
-                          "and step i's output copied on their own streams while step i runs"},
+                "copies": E2E_COPIES},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "sustained": sustained,
@@ -564,9 +580,15 @@ def run_gpu_linear(args) -> None:
     q, k, v = (ys[0].view(tokens, 32, 128), ys[1].view(tokens, 8, 128), ys[2].view(tokens, 8, 128))
     stream = torch.cuda.Stream(device=dev)
 
-    def step():
-        pool.qkv_proj(x, w_qkv, q, k, v, stream=stream)
-        pool.linear(a, ws[3], ys[3], stream=stream)
+    def make_step(xb, ab, yb):
+        qb, kb, vb = (yb[0].view(tokens, 32, 128), yb[1].view(tokens, 8, 128), yb[2].view(tokens, 8, 128))
+
+        def run():
+            pool.qkv_proj(xb, w_qkv, qb, kb, vb, stream=stream)
+            pool.linear(ab, ws[3], yb[3], stream=stream)
+        return run
+
+    step = make_step(x, a, ys)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -601,22 +623,14 @@ def run_gpu_linear(args) -> None:
     pkv.pkv_timer_enable(pool.handle, False)
 
     host_in = [host_x.pin_memory(), host_a.pin_memory()]
-    host_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys]
+    host_out = [[torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    x2, a2, ys2 = x.clone(), a.clone(), [torch.empty_like(y) for y in ys]
+    sets = [([x, a], make_step(x, a, ys), ys, host_out[0]), ([x2, a2], make_step(x2, a2, ys2), ys2, host_out[1])]
     barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            flush()
-            x.copy_(host_in[0], non_blocking=True)
-            a.copy_(host_in[1], non_blocking=True)
-            step()
-            for h, y in zip(host_out, ys):
-                h.copy_(y, non_blocking=True)
-        stream.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_s = double_buffered_e2e(args.steps, sets, host_in, flush, stream, dev)
+    e2e_s = max_over_ranks(e2e_s, world)
     flags = pkv.pkv_check_errors(pool.handle, stream)
     if flags:
         raise SystemExit(f"device error flags {flags}")
@@ -659,7 +673,7 @@ def run_gpu_linear(args) -> None:
                    "parallelism": f"dp{world} (independent replicas)"},
         "roofline": roofline,
         "e2e": {"value": tokens * args.steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "copies": E2E_COPIES},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "gpu": torch.cuda.get_device_name(dev),
@@ -710,10 +724,14 @@ def run_gpu_layer(args) -> None:
     ws = pool.workspace(R, pages, 0)
     stream = torch.cuda.Stream(device=dev)
 
-    def step_fused():
-        pkv.pkv_qkv_proj_append(pool.handle, x, w_qkv, qw, kw, pos, tab, q_hat, stream)
-        pkv.pkv_decode_appended(pool.handle, q_hat, pos, tab, attn, ws, stream)
-        pkv.pkv_linear(pool.handle, attn.view(R, hidden), w_o, y, None, stream)
+    def make_fused(xb, yb):
+        def run():
+            pkv.pkv_qkv_proj_append(pool.handle, xb, w_qkv, qw, kw, pos, tab, q_hat, stream)
+            pkv.pkv_decode_appended(pool.handle, q_hat, pos, tab, attn, ws, stream)
+            pkv.pkv_linear(pool.handle, attn.view(R, hidden), w_o, yb, None, stream)
+        return run
+
+    step_fused = make_fused(x, y)
 
     def step_unfused():
         pkv.pkv_qkv_proj(pool.handle, x, w_qkv, q, k, v, stream)
@@ -752,18 +770,13 @@ def run_gpu_layer(args) -> None:
         sustained = sustained_pass(step_fused, None, stream, ms_step, args.sustain_seconds)
     barrier(world)
 
-    host_in = host_x.pin_memory()
-    host_out = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    host_in = [host_x.pin_memory()]
+    host_out = [[torch.empty(y.shape, dtype=y.dtype, pin_memory=True)] for _ in range(2)]
+    x2, y2 = x.clone(), torch.empty_like(y)
+    sets = [([x], make_fused(x, y), [y], host_out[0]), ([x2], make_fused(x2, y2), [y2], host_out[1])]
     barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            x.copy_(host_in, non_blocking=True)
-            step_fused()
-            host_out.copy_(y, non_blocking=True)
-        stream.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_s = double_buffered_e2e(args.steps, sets, host_in, None, stream, dev)
+    e2e_s = max_over_ranks(e2e_s, world)
     if pkv.pkv_check_errors(pool.handle, stream):
         raise SystemExit("device error flags")
 
@@ -801,8 +814,8 @@ def run_gpu_layer(args) -> None:
                      "timed_launches": attn_n,
                      "timing": "CUDA events around each attention launch, a separate pass of the same steps"},
         "layer_gbs": (kv + weight_bytes) / (ms_step / 1e3) / 1e9,
-        "e2e": {"value": R * args.steps * world / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": host_in.numel() * 2,
-                "d2h_bytes_per_step": host_out.numel() * 2},
+        "e2e": {"value": R * args.steps * world / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": host_in[0].numel() * 2,
+                "d2h_bytes_per_step": host_out[0][0].numel() * 2, "copies": E2E_COPIES},
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
         "sustained": sustained,
