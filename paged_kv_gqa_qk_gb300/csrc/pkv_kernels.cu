@@ -1140,6 +1140,7 @@ struct CombineParams {
 
 // One CTA per (token, kv head) unit; warp w = query head 4g+w, lane owns dims 4*lane..4*lane+3.
 //   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M)   over the unit's pieces c
+template <int kBatch>
 __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1199,18 +1200,27 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
         acc[2] += w * ob[k].z;
         acc[3] += w * ob[k].w;
     }
+    // the rest in batches of kBatch whose loads are all issued before the first is summed
+    // (a unit split over many chunks, as a few long rows are, would otherwise pay a round
+    // trip every few pieces); the sum still runs in piece order
     for (int r0 = 0; r0 < np; r0 += 32) {
         const int nb = min(32, np - r0);
         const float wl = r0 == 0 ? wl0 : (lane < nb ? exp2f(lse[(int64_t)(r0 + lane) * kGroup] - M) : 0.f);
-#pragma unroll 4
-        for (int r = r0 == 0 ? kPre : 0; r < nb; ++r) {
-            const float w = __shfl_sync(kFull, wl, r);
-            const float4 o = *reinterpret_cast<const float4*>(po + (r0 + r) * ostride);
-            wsum += w;
-            acc[0] += w * o.x;
-            acc[1] += w * o.y;
-            acc[2] += w * o.z;
-            acc[3] += w * o.w;
+        for (int r = r0 == 0 ? kPre : 0; r < nb; r += kBatch) {
+            float4 o[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (r + i < nb) o[i] = *reinterpret_cast<const float4*>(po + (r0 + r + i) * ostride);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                if (r + i >= nb) break;  // the same on every lane
+                const float w = __shfl_sync(kFull, wl, r + i);
+                wsum += w;
+                acc[0] += w * o[i].x;
+                acc[1] += w * o[i].y;
+                acc[2] += w * o[i].z;
+                acc[3] += w * o[i].w;
+            }
         }
     }
     const float inv = 1.f / wsum;
@@ -1245,7 +1255,12 @@ cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+    // Few units for the grid (a few long rows): each is split over many chunks, and the
+    // combine's CTAs are few, so each loads 16 pieces at a time.  Otherwise 8 at a time
+    // keep the kernel at 64 registers, two of its CTAs resident beside the attention's.
+    const int64_t units = (int64_t)plan.tokens * pool->cfg.kv_heads;
+    if (units < 2 * (int64_t)plan.ctas) return cudaLaunchKernelEx(&cfg, combine_kernel<16>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<8>, p);
 }
 
 // =====================================================================================
