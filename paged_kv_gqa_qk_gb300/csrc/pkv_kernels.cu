@@ -1140,14 +1140,17 @@ struct CombineParams {
 
 // One CTA per (token, kv head) unit; warp w = query head 4g+w, lane owns dims 4*lane..4*lane+3.
 //   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M)   over the unit's pieces c
-template <int kBatch>
-__global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
+template <int kBatch, int kWph>
+__global__ void __launch_bounds__(128 * kWph) combine_kernel(CombineParams p)
 {
+    // warp w merges query head w % 4 of the unit's kv group; with kWph warps a
+    // head, warp w takes every kWph-th piece from piece w / 4 on
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hw = warp % kGroup, sub = warp / kGroup;
     const int G = p.kv_heads;
     const int u = blockIdx.x;
     const int t = u / G, g = u % G;
-    const int h = g * kGroup + warp;
+    const int h = g * kGroup + hw;
     pdl_wait();
     if (u == 0 && threadIdx.x == 0) *p.claim = 0;  // the attention grid has finished claiming
     __nv_bfloat16* dst = p.out + ((int64_t)t * p.heads + h) * kHeadDim + 4 * lane;
@@ -1156,7 +1159,7 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
     const int uok = p.unit_ok[u];
     const int n = pre1 - pre;
     if (n == 0) {  // skipped token
-        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        if (sub == 0) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
         if (p.decode_mode && g == 0 && threadIdx.x == 0) {
             const int pos = p.positions[t];
             if (pos != -1) atomicOr(p.err, PKV_DEVERR_POSITION);
@@ -1164,7 +1167,7 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
         return;
     }
     if (!uok) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        if (sub == 0) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
         return;
     }
     const int64_t T = (int64_t)G * total;
@@ -1172,19 +1175,24 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
     const int64_t S = (int64_t)G * pre + (int64_t)g * n;
     const int64_t rf = interval_of(S, sp), rl = interval_of(S + n - 1, sp);
     if (rf == rl) return;  // one interval held the whole unit, and its CTA wrote it out
-    // the pieces' log-sum-exps, one per lane, and the first kPre pieces' partial
-    // outputs, all in flight together (a second round trip); then the rest of
-    // the outputs in piece order, batches of independent loads
+    // the pieces' log-sum-exps, one per lane, and this warp's first kPre pieces'
+    // partial outputs, all in flight together (a second round trip); then the
+    // rest of this warp's pieces in order, in batches of kBatch whose loads are
+    // all issued before the first is summed (a unit split over many chunks, as a
+    // few long rows are, would otherwise pay a round trip every few pieces)
     constexpr int kPre = 4;
+    static_assert(kPre * kWph <= 32 && 32 % kWph == 0, "the first pieces lie in the first block of 32");
     const int np = (int)(rl - rf + 1);
-    const float* lse = p.part_lse + ((int64_t)u + rf) * kGroup + warp;
-    const float* po = p.part_o + (((int64_t)u + rf) * kGroup + warp) * kHeadDim + 4 * lane;
+    const float* lse = p.part_lse + ((int64_t)u + rf) * kGroup + hw;
+    const float* po = p.part_o + (((int64_t)u + rf) * kGroup + hw) * kHeadDim + 4 * lane;
     const int64_t ostride = (int64_t)kGroup * kHeadDim;
     const float l0 = lane < np ? lse[(int64_t)lane * kGroup] : -CUDART_INF_F;
     float4 ob[kPre];
 #pragma unroll
-    for (int k = 0; k < kPre; ++k)
-        ob[k] = k < np ? *reinterpret_cast<const float4*>(po + k * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kPre; ++k) {
+        const int r = sub + k * kWph;
+        ob[k] = r < np ? *reinterpret_cast<const float4*>(po + r * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float M = l0;
     for (int r = lane + 32; r < np; r += 32) M = fmaxf(M, lse[(int64_t)r * kGroup]);
 #pragma unroll
@@ -1193,34 +1201,43 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineParams p)
     float wsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {  // pieces beyond np add w = 0 times o = 0
-        const float w = __shfl_sync(kFull, wl0, k);
+        const float w = __shfl_sync(kFull, wl0, sub + k * kWph);
         wsum += w;
         acc[0] += w * ob[k].x;
         acc[1] += w * ob[k].y;
         acc[2] += w * ob[k].z;
         acc[3] += w * ob[k].w;
     }
-    // the rest in batches of kBatch whose loads are all issued before the first is summed
-    // (a unit split over many chunks, as a few long rows are, would otherwise pay a round
-    // trip every few pieces); the sum still runs in piece order
     for (int r0 = 0; r0 < np; r0 += 32) {
         const int nb = min(32, np - r0);
         const float wl = r0 == 0 ? wl0 : (lane < nb ? exp2f(lse[(int64_t)(r0 + lane) * kGroup] - M) : 0.f);
-        for (int r = r0 == 0 ? kPre : 0; r < nb; r += kBatch) {
+        for (int r = r0 == 0 ? sub + kPre * kWph : sub; r < nb; r += kWph * kBatch) {
             float4 o[kBatch];
 #pragma unroll
             for (int i = 0; i < kBatch; ++i)
-                if (r + i < nb) o[i] = *reinterpret_cast<const float4*>(po + (r0 + r + i) * ostride);
+                if (r + i * kWph < nb) o[i] = *reinterpret_cast<const float4*>(po + (r0 + r + i * kWph) * ostride);
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
-                if (r + i >= nb) break;  // the same on every lane
-                const float w = __shfl_sync(kFull, wl, r + i);
+                if (r + i * kWph >= nb) break;  // the same on every lane
+                const float w = __shfl_sync(kFull, wl, r + i * kWph);
                 wsum += w;
                 acc[0] += w * o[i].x;
                 acc[1] += w * o[i].y;
                 acc[2] += w * o[i].z;
                 acc[3] += w * o[i].w;
             }
+        }
+    }
+    if constexpr (kWph > 1) {  // the head's warps' sums, added in warp order
+        __shared__ float part[kWph][kGroup][32][5];
+        float* mine = part[sub][hw][lane];
+        mine[0] = acc[0], mine[1] = acc[1], mine[2] = acc[2], mine[3] = acc[3], mine[4] = wsum;
+        __syncthreads();
+        if (sub != 0) return;
+#pragma unroll
+        for (int q = 1; q < kWph; ++q) {
+            const float* o = part[q][hw][lane];
+            acc[0] += o[0], acc[1] += o[1], acc[2] += o[2], acc[3] += o[3], wsum += o[4];
         }
     }
     const float inv = 1.f / wsum;
@@ -1256,11 +1273,16 @@ cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // Few units for the grid (a few long rows): each is split over many chunks, and the
-    // combine's CTAs are few, so each loads 16 pieces at a time.  Otherwise 8 at a time
-    // keep the kernel at 64 registers, two of its CTAs resident beside the attention's.
+    // combine's CTAs are few, so each loads 16 pieces at a time, and under half a unit a
+    // CTA, four warps share each query head.  Otherwise 8 at a time keep the kernel at 64
+    // registers, two of its CTAs resident beside the attention's.
     const int64_t units = (int64_t)plan.tokens * pool->cfg.kv_heads;
-    if (units < 2 * (int64_t)plan.ctas) return cudaLaunchKernelEx(&cfg, combine_kernel<16>, p);
-    return cudaLaunchKernelEx(&cfg, combine_kernel<8>, p);
+    if (2 * units < (int64_t)plan.ctas) {
+        cfg.blockDim = dim3(128 * 4);
+        return cudaLaunchKernelEx(&cfg, combine_kernel<16, 4>, p);
+    }
+    if (units < 2 * (int64_t)plan.ctas) return cudaLaunchKernelEx(&cfg, combine_kernel<16, 1>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<8, 1>, p);
 }
 
 // =====================================================================================
