@@ -196,10 +196,11 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t vs, int h, int 
 }
 
 // Every role runs its own unit loop through the same four CTA barriers per
-// unit: (1) the unit the producer claimed is visible, (2) the tile's tokens
-// are loaded, (3) its runs and Q are ready, (4) every product of the unit has
-// completed (the epilogues waited for the last one), so that the next unit may
-// rewrite Q and the token table.
+// unit: (1) the unit the producer claimed is visible (and the producer has
+// requested its Q, whose landing the issuer waits for on q_full), (2) the
+// tile's tokens are loaded, (3) its runs are ready, (4) every product of the
+// unit has completed (the epilogues waited for the last one), so that the next
+// unit may rewrite Q and the token table.
 
 // ---------------------------------------------------------------- producer (warp 8)
 __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p, const CUtensorMap* tmK,
