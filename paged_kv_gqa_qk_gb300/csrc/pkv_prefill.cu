@@ -211,10 +211,9 @@ __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p,
     int q_units = 0;  // units whose Q has been requested
     const uint64_t pol = l2_policy_evict_last();    // a prompt's tiles re-read the same pages
     const uint64_t pol_q = l2_policy_evict_first();  // each unit's Q is read once
-    bool first = true;
+    int claim = first_claim;  // the next unit, claimed before it is needed
     for (;;) {
-        if (lane == 0) *c.sUnit = first ? first_claim : atomicAdd(p.sched, 1);
-        first = false;
+        if (lane == 0) *c.sUnit = claim;
         __syncthreads();  // (1)
         const int u = *c.sUnit;
         if (u >= c.nunits || *c.abort_flag) break;
@@ -280,6 +279,10 @@ __device__ __forceinline__ void producer_role(const PfCtx& c, const PfParams& p,
                 }
             }
         }
+        // the next unit is claimed once this one's last copy is out, about two blocks before
+        // it ends: the counter's answer is back by then, and the units still go, longest
+        // first, to the CTAs about to be free
+        if (lane == 0) claim = atomicAdd(p.sched, 1);
         if (!ok && lane == 0) {
             atomicOr(p.err, PKV_DEVERR_TIMEOUT);
             *c.abort_flag = 1;
