@@ -15,7 +15,8 @@
 //                   several CTAs shared; zero outputs for skipped tokens.
 //   prep_kernel     step mode only: validates every token and appends all k/v
 //                   before any attention (the prompt tokens of a chunk read
-//                   each other's keys).
+//                   each other's keys), and writes each prompt token's query
+//                   heads, normed, roped and scaled, for the prompt attention.
 //
 // Source of the computation: qwen3-8b Nest files, src/attention.linnet,
 // GroupedQueryAttention.decode_paged / step_paged (q_norm/k_norm -> rope_rows
