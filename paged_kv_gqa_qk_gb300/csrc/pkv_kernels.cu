@@ -379,8 +379,9 @@ struct AttnSmem {
     static constexpr int kM = kSide + kStages * kSideBytes;  // float [4 warps][4 heads]
     static constexpr int kL = kM + 64;                        // float [4][4]
     static constexpr int kMeta = kL + 64;                     // int4 [stages][2]
-    static constexpr int kScan = kMeta + kStages * 32;        // int [8]
+    static constexpr int kScan = kMeta + kStages * 32;        // int [8]: warp sums [5], -, first token and its prefix
     static constexpr int kSum = kScan + 32;                   // int [threads] first token, int [threads] prefix
+    static_assert(kAttnThreads / 32 <= 6, "the warp sums leave the scan's last two ints free");
     static constexpr int kW = kSum + 2 * kAttnThreads * 4;    // bf16 q_norm_w [128], k_norm_w [128]
     static constexpr int kBars = kW + 512;                    // u64 full[S], empty[S], group
     static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);  // int abort, items issued, stop item sent
@@ -606,6 +607,24 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int excl = warp_base + incl - local;
     sT0[tid] = t0;
     sP0[tid] = excl;
+    const int64_t T = (int64_t)G * total;
+    const Split sp = split_of(T, C);  // never more slices than pages: none is empty
+    if (c < sp.Ce) {
+        // the token holding this CTA's first page (and its prefix), found by the one
+        // thread whose run of tokens holds it, so that the producer starts without a search
+        const int64_t x0 = (int64_t)c * sp.S / sp.Ce;
+        int run = excl;
+        if (x0 >= (int64_t)G * run && x0 < (int64_t)G * (run + local))
+            for (int t = t0; t < t1; ++t) {
+                const int n = npg_of(p, t);
+                if (n > 0 && x0 < (int64_t)G * (run + n)) {
+                    sScan[6] = t;
+                    sScan[7] = run;
+                    break;
+                }
+                run += n;
+            }
+    }
     if (c == 0) {
         int run = excl;
         for (int t = t0; t < t1; ++t) {
@@ -615,8 +634,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         if (tid == kAttnThreads - 1) p.prefix[nt] = total;
     }
     __syncthreads();
-    const int64_t T = (int64_t)G * total;
-    const Split sp = split_of(T, C);  // never more slices than pages: none is empty
     if (c >= sp.Ce) {
         if (p.late_wait) pdl_wait();
         return;
@@ -639,7 +656,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         bool want = sp.ND > 0;  // the next chunk is still to be claimed
         for (;;) {
             int t, pre;
-            find_token(p, sT0, sP0, xb, lane, t, pre);
+            if (iv == c) {  // the static slice: its first token was found in the prologue
+                t = sScan[6];
+                pre = sScan[7];
+            } else {
+                find_token(p, sT0, sP0, xb, lane, t, pre);
+            }
             int64_t St = (int64_t)G * pre;  // global index of (t, kv head 0, page 0)
             int64_t x = xb;
             while (x < xe && ok) {
@@ -650,6 +672,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                 int row, len;
                 token_info(p, t, row, len);
                 const int pos = len - 1;
+                // lane 0: the table entry of page jj; lanes 1 and 2: the same column of the rows
+                // before and after, so that a prefix page shared with a neighbouring row is known
+                auto entries = [&](int jj) {
+                    int e = -1;
+                    if (lane < 3) {
+                        const int r2 = row + (lane == 0 ? 0 : (lane == 1 ? -1 : 1));
+                        if (lane == 0 || (p.table && r2 >= 0 && r2 < p.rows)) e = page_of(p.table, p.pages, r2, jj);
+                    }
+                    return e;
+                };
+                int pg_next = entries(j);  // loaded together with the row check's entries
                 bool valid = true;
                 if (p.decode_mode) {  // every page the row will read must be a pool page
                     int bad = 0;
@@ -679,13 +712,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                         ok = false;
                         break;
                     }
-                    // lane 0: the page; lanes 1 and 2: the same column of the rows before and
-                    // after, so that a prefix page shared with a neighbouring row is known
-                    int pg = -1;
-                    if (valid && lane < 3) {
-                        const int r2 = row + (lane == 0 ? 0 : (lane == 1 ? -1 : 1));
-                        if (lane == 0 || (p.table && r2 >= 0 && r2 < p.rows)) pg = page_of(p.table, p.pages, r2, jj);
-                    }
+                    const int pg = valid ? pg_next : -1;
+                    if (s + 1 < seg) pg_next = entries(jj + 1);  // in flight while the next stage frees up
                     const int page = max(__shfl_sync(kFull, pg, 0), 0);
                     const int pprev = __shfl_sync(kFull, pg, 1), pnext = __shfl_sync(kFull, pg, 2);
                     const uint64_t ppol = (pprev == page || pnext == page) ? pol_shared : pol;

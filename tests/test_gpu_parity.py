@@ -63,6 +63,24 @@ def test_ragged_lengths_and_partitions(ctas):
     compare(wl, run_gpu(wl, ctas=ctas), run_oracle(wl), label=f"ragged ctas={ctas}")
 
 
+@pytest.mark.parametrize("ctas", [0, 7])
+def test_last_positions_of_the_context(ctas):
+    """The largest positions the configuration allows (max_seq 40960: page 639,
+    slot 63): decode rows whose step token is the context's last position, one
+    page before it and at its first page, beside short rows."""
+    wl = W.make_decode("max_seq", [40960, 1, 40960 - 64, 40897, 7], seed=27, table_pages=640)
+    compare(wl, run_gpu(wl, ctas=ctas), run_oracle(wl), label=f"max_seq ctas={ctas}")
+
+
+def test_step_prompt_ending_at_the_last_position():
+    """A prompt chunk whose last token sits at position 40959 (the prompt
+    attention's longest run, a tile ending on the context's last slot), a
+    3-token chunk ending there too, and a decode row at the same position."""
+    wl = W.make_step("max_seq step", prompt_lengths=[40, 3], prompt_starts=[40920, 40957],
+                     decode_lengths=[40960, 7], seed=28, table_pages=640)
+    compare(wl, run_gpu(wl), run_oracle(wl), label="max_seq step")
+
+
 def test_sweep_shape_small():
     wl = W.sweep(8, 4096, seed=5)
     compare(wl, run_gpu(wl), run_oracle(wl), label="sweep 8x4096")
