@@ -348,7 +348,7 @@ struct AttnParams {
     float* part_lse;          // [U + C (1 + kDynChunksPerCta)][4]
     uint32_t* claim;          // chunk counter, zero at launch
     int32_t* prefix;          // [ntok + 1], written by CTA 0 for combine_kernel
-    int32_t* unit_ok;         // [U], written by the CTA holding each unit's first page
+    int32_t* unit_ok;         // [U], by the CTA holding each unit's first page: 0 invalid, 1 cut, 2 written out
     uint32_t* err;
     int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode, rot;
     int rows;                 // table rows (for the neighbouring-row comparison of shared pages)
@@ -379,10 +379,13 @@ struct AttnSmem {
     static constexpr int kM = kSide + kStages * kSideBytes;  // float [4 warps][4 heads]
     static constexpr int kL = kM + 64;                        // float [4][4]
     static constexpr int kMeta = kL + 64;                     // int4 [stages][2]
-    static constexpr int kScan = kMeta + kStages * 32;        // int [8]: warp sums [5], -, first token and its prefix
-    static constexpr int kSum = kScan + 32;                   // int [threads] first token, int [threads] prefix
-    static_assert(kAttnThreads / 32 <= 6, "the warp sums leave the scan's last two ints free");
-    static constexpr int kW = kSum + 2 * kAttnThreads * 4;    // bf16 q_norm_w [128], k_norm_w [128]
+    // int [32]: per warp the page sums [0, 8), the largest unit [8, 16) and the tokens
+    // with pages [16, 24); the first token of the CTA's slice and its prefix at 24, 25
+    static constexpr int kScan = kMeta + kStages * 32;
+    static constexpr int kSum = kScan + 128;                  // int [threads] first token, int [threads] prefix
+    static_assert(kAttnThreads / 32 <= 8, "a warp's entries of the scan fit");
+    static constexpr int kN = kSum + 2 * kAttnThreads * 4;    // int [threads]: pages per token (whole-unit split)
+    static constexpr int kW = kN + kAttnThreads * 4;          // bf16 q_norm_w [128], k_norm_w [128]
     static constexpr int kBars = kW + 512;                    // u64 full[S], empty[S], group
     static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);  // int abort, items issued, stop item sent
     static constexpr int kBytes = kFlag + 16;
@@ -410,6 +413,7 @@ struct Split {
     int Ce;     // static slices (CTAs with work)
     int ND;     // chunks after them
     int Q;      // pages per chunk
+    int whole;  // whole units instead (see whole_split): Ce first units, then ND claimed ones
 };
 
 __device__ __forceinline__ Split split_of(int64_t T, int C)
@@ -419,12 +423,41 @@ __device__ __forceinline__ Split split_of(int64_t T, int C)
     sp.S = T;
     sp.ND = 0;
     sp.Q = kDynChunkPages;
+    sp.whole = 0;
     if (sp.Ce > 1 && T >= (int64_t)kDynMinPagesPerCta * sp.Ce) {
         const int64_t dyn = T / 4, cap = (int64_t)kDynChunksPerCta * sp.Ce;
         sp.Q = (int)max((int64_t)kDynChunkPages, (dyn + cap - 1) / cap);
         sp.ND = (int)(dyn / sp.Q);
         sp.S = T - (int64_t)sp.ND * sp.Q;
     }
+    return sp;
+}
+
+// The whole-unit split, for calls of short rows: when every token has a thread
+// of the prologue (ntok <= kAttnThreads), no unit is longer than
+// kWholeMaxPages and the longest is within 5/4 of a CTA's share of the pages,
+// no unit is cut at all.  The units go out longest first (tokens ordered by
+// their page count, ties by index; a token's kv heads in order): CTA c takes
+// unit c, and the rest are claimed one at a time from the chunk counter.  Each
+// unit is then one segment, written out by the CTA that streams it, and the
+// last units handed out are the shortest; with slices and chunks a call of
+// short rows pays several segments a CTA (a preparation of q at the start of
+// each, a merge and a partial at its end) and a tail of a whole chunk.
+constexpr int kWholeMaxPages = 16;
+
+__device__ __forceinline__ bool whole_units(int ntok, int nmax, int64_t T, int C)
+{
+    return ntok <= kAttnThreads && nmax <= kWholeMaxPages && 4 * (int64_t)nmax * C <= 5 * T;
+}
+
+__device__ __forceinline__ Split whole_split(int units, int C)
+{
+    Split sp;
+    sp.Ce = min(C, units);
+    sp.ND = units - sp.Ce;
+    sp.S = 0;
+    sp.Q = 0;
+    sp.whole = 1;
     return sp;
 }
 
@@ -542,6 +575,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     int* sScan = reinterpret_cast<int*>(sbase + L::kScan);
     int* sT0 = reinterpret_cast<int*>(sbase + L::kSum);
     int* sP0 = sT0 + kAttnThreads;
+    int* sN = reinterpret_cast<int*>(sbase + L::kN);
     uint2* sW = reinterpret_cast<uint2*>(sbase + L::kW);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -587,43 +621,70 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int nt = p.ntok;
     const int per = (nt + kAttnThreads - 1) / kAttnThreads;
     const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
-    int local = 0;
-    for (int t = t0; t < t1; ++t) local += npg_of(p, t);
-    int incl = local;
+    int local = 0, lmax = 0, lnz = 0;  // pages, the longest unit, tokens with pages
+    for (int t = t0; t < t1; ++t) {
+        const int n = npg_of(p, t);
+        local += n;
+        lmax = max(lmax, n);
+        lnz += n > 0;
+    }
+    if (per == 1) sN[tid] = local;  // (read only when every token has its own thread)
+    int incl = local, wmax = lmax, wnz = lnz;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(kFull, incl, o);
         if (lane >= o) incl += y;
+        wmax = max(wmax, __shfl_xor_sync(kFull, wmax, o));
+        wnz += __shfl_xor_sync(kFull, wnz, o);
     }
-    if (lane == 31) sScan[warp] = incl;
+    if (lane == 31) {
+        sScan[warp] = incl;
+        sScan[8 + warp] = wmax;
+        sScan[16 + warp] = wnz;
+    }
     __syncthreads();
-    int total = 0, warp_base = 0;
+    int total = 0, warp_base = 0, nmax = 0, nz = 0;
 #pragma unroll
     for (int w = 0; w < kAttnThreads / 32; ++w) {
         const int v = sScan[w];
         warp_base += (w < warp) ? v : 0;
         total += v;
+        nmax = max(nmax, sScan[8 + w]);
+        nz += sScan[16 + w];
     }
     const int excl = warp_base + incl - local;
-    sT0[tid] = t0;
-    sP0[tid] = excl;
     const int64_t T = (int64_t)G * total;
-    const Split sp = split_of(T, C);  // never more slices than pages: none is empty
-    if (c < sp.Ce) {
-        // the token holding this CTA's first page (and its prefix), found by the one
-        // thread whose run of tokens holds it, so that the producer starts without a search
-        const int64_t x0 = (int64_t)c * sp.S / sp.Ce;
-        int run = excl;
-        if (x0 >= (int64_t)G * run && x0 < (int64_t)G * (run + local))
-            for (int t = t0; t < t1; ++t) {
-                const int n = npg_of(p, t);
-                if (n > 0 && x0 < (int64_t)G * (run + n)) {
-                    sScan[6] = t;
-                    sScan[7] = run;
-                    break;
-                }
-                run += n;
+    const Split sp = whole_units(nt, nmax, T, C) ? whole_split(G * nz, C) : split_of(T, C);
+    if (sp.whole) {
+        // tokens longest first (ties by index): sT0[rank] = the token, sP0[rank] = its prefix
+        if (tid < nt && local > 0) {
+            int rank = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int m = sN[t];
+                rank += (m > local) || (m == local && t < tid);
             }
+            sT0[rank] = tid;
+            sP0[rank] = excl;
+        }
+    } else {
+        sT0[tid] = t0;
+        sP0[tid] = excl;
+        if (c < sp.Ce) {
+            // the token holding this CTA's first page (and its prefix), found by the one
+            // thread whose run of tokens holds it, so that the producer starts without a search
+            const int64_t x0 = (int64_t)c * sp.S / sp.Ce;
+            int run = excl;
+            if (x0 >= (int64_t)G * run && x0 < (int64_t)G * (run + local))
+                for (int t = t0; t < t1; ++t) {
+                    const int n = npg_of(p, t);
+                    if (n > 0 && x0 < (int64_t)G * (run + n)) {
+                        sScan[24] = t;
+                        sScan[25] = run;
+                        break;
+                    }
+                    run += n;
+                }
+        }
     }
     if (c == 0) {
         int run = excl;
@@ -646,19 +707,32 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         // Pages are read once, except the pages several rows share (a shared prompt
         // prefix): those stay in L2 for the other rows' reads, the rest go first.
         const uint64_t pol = l2_policy_evict_first(), pol_shared = l2_policy_evict_last();
-        // the static slice, then one claimed chunk after another.  A chunk is
-        // claimed when the range before it has kClaimAhead pages left to issue:
-        // late enough that the CTAs finishing first take the chunks, early enough
-        // that the counter's answer is there when the range ends.
-        int64_t xb = (int64_t)c * sp.S / sp.Ce, xe = (int64_t)(c + 1) * sp.S / sp.Ce;
-        int iv = c;  // the range's interval: partials of its pieces go to u + iv
+        // the static slice, then one claimed chunk after another (whole-unit split:
+        // unit c, then one claimed unit after another).  A chunk is claimed when
+        // the range before it has kClaimAhead pages left to issue: late enough that
+        // the CTAs finishing first take the chunks, early enough that the
+        // counter's answer is there when the range ends.
+        int64_t xb = 0, xe = 0;
+        if (!sp.whole) {
+            xb = (int64_t)c * sp.S / sp.Ce;
+            xe = (int64_t)(c + 1) * sp.S / sp.Ce;
+        }
+        int iv = c;     // the range's interval: partials of its pieces go to u + iv
+        int unit = c;   // whole-unit split: the range's unit, in longest-first order
         uint32_t claim = 0;
         bool want = sp.ND > 0;  // the next chunk is still to be claimed
         for (;;) {
             int t, pre;
-            if (iv == c) {  // the static slice: its first token was found in the prologue
-                t = sScan[6];
-                pre = sScan[7];
+            if (sp.whole) {  // one unit, never cut: no partials
+                t = sT0[unit / G];
+                pre = sP0[unit / G];
+                const int n = sN[t];
+                xb = (int64_t)G * pre + (int64_t)(unit % G) * n;
+                xe = xb + n;
+                iv = 0;
+            } else if (iv == c) {  // the static slice: its first token was found in the prologue
+                t = sScan[24];
+                pre = sScan[25];
             } else {
                 find_token(p, sT0, sP0, xb, lane, t, pre);
             }
@@ -693,8 +767,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                     valid = !__any_sync(kFull, bad);
                 }
                 const int u = t * G + g;
-                if (j == 0 && lane == 0) {
-                    p.unit_ok[u] = valid ? 1 : 0;
+                if (j == 0 && lane == 0) {  // 2: the unit is this range's alone, written out here
+                    p.unit_ok[u] = valid ? (j + seg == n ? 2 : 1) : 0;
                     if (!valid && g == 0) atomicOr(p.err, PKV_DEVERR_PAGE);
                 }
                 const bool has_last = j + seg == n;
@@ -763,6 +837,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             want = true;
             const uint32_t k = __shfl_sync(kFull, claim, 0);
             if (k >= (uint32_t)sp.ND) break;
+            unit = sp.Ce + (int)k;
             xb = sp.S + (int64_t)k * sp.Q;
             xe = xb + sp.Q;
             iv = sp.Ce + (int)k;
@@ -1199,6 +1274,7 @@ __global__ void __launch_bounds__(128 * kWph) combine_kernel(CombineParams p)
         if (sub == 0) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
         return;
     }
+    if (uok == 2) return;  // one range held the whole unit, and its CTA wrote it out
     const int64_t T = (int64_t)G * total;
     const Split sp = split_of(T, p.ctas);  // the attention kernel's intervals
     const int64_t S = (int64_t)G * pre + (int64_t)g * n;

@@ -142,6 +142,41 @@ def test_claimed_chunks_give_the_same_bits_every_call():
     pool.close()
 
 
+def _streams_units_whole(wl, ctas, step_positions, pages):
+    """The attention's rule for handing out every (token, kv head) unit whole,
+    longest first: at most one token per prologue thread (160), no unit longer
+    than 16 pages, the longest within 5/4 of a CTA's share of all pages."""
+    S, G = wl.cfg["page_size"], wl.cfg["kv_heads"]
+    npg = [p // S + 1 for p in step_positions.tolist() if 0 <= p < min(wl.cfg["max_seq"], pages * S)]
+    C = ctas or 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    T = G * sum(npg)
+    return len(step_positions) <= 160 and max(npg) <= 16 and 4 * max(npg) * C <= 5 * T
+
+
+@pytest.mark.parametrize("rows", [64, 160, 161])
+def test_short_rows_streamed_as_whole_units(rows):
+    """Calls of short rows: with at most 160 rows, no unit above 16 pages and the
+    longest within 5/4 of a CTA's share, each (token, kv head) is streamed whole
+    by one CTA, longest first, and written out by it; the output then does not
+    depend on the grid size.  A skipped row and a row with an invalid page sit
+    among them; 161 rows take the slices and chunks instead."""
+    wl = W.make_decode("short rows", (rows, 1, 1024), seed=40 + rows, table_pages=16)
+    sp = wl.step_positions.clone()
+    table = wl.table.clone()
+    sp[3] = -1                        # no step
+    table[5, 0] = wl.num_pages + 3    # not a pool page
+    ref = run_oracle(wl, table=table, step_positions=sp)
+    outs = []
+    for ctas in (0, 2, 7, 1):
+        whole = _streams_units_whole(wl, ctas, sp, table.shape[1])
+        assert whole == (rows <= 160), (rows, ctas)
+        gpu = run_gpu(wl, ctas=ctas, table=table, step_positions=sp)
+        compare(wl, gpu, ref, label=f"short rows {rows} ctas={ctas}")
+        outs.append(gpu[0])
+    if rows <= 160:
+        assert all(torch.equal(o, outs[0]) for o in outs[1:])
+
+
 # ------------------------------------------------------------------ skipped tokens and device errors
 
 def test_inactive_and_invalid_rows():
