@@ -384,8 +384,11 @@ struct AttnSmem {
     static constexpr int kScan = kMeta + kStages * 32;
     static constexpr int kSum = kScan + 128;                  // int [threads] first token, int [threads] prefix
     static_assert(kAttnThreads / 32 <= 8, "a warp's entries of the scan fit");
-    static constexpr int kN = kSum + 2 * kAttnThreads * 4;    // int [threads]: pages per token (whole-unit split)
-    static constexpr int kW = kN + kAttnThreads * 4;          // bf16 q_norm_w [128], k_norm_w [128]
+    // int [threads] each: pages, length and table row per token (read by the whole-unit split)
+    static constexpr int kTokN = kSum + 2 * kAttnThreads * 4;
+    static constexpr int kTokLen = kTokN + kAttnThreads * 4;
+    static constexpr int kTokRow = kTokLen + kAttnThreads * 4;
+    static constexpr int kW = kTokRow + kAttnThreads * 4;     // bf16 q_norm_w [128], k_norm_w [128]
     static constexpr int kBars = kW + 512;                    // u64 full[S], empty[S], group
     static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);  // int abort, items issued, stop item sent
     static constexpr int kBytes = kFlag + 16;
@@ -476,15 +479,19 @@ __device__ __forceinline__ int interval_of(int64_t x, const Split& sp)
     return x < sp.S ? cta_of(x, sp.S, sp.Ce) : sp.Ce + (int)((x - sp.S) / sp.Q);
 }
 
-__device__ __forceinline__ int npg_of(const AttnParams& p, int t)
+// What token t's page count comes from: its position (decode mode) or its length.
+__device__ __forceinline__ int tok_value(const AttnParams& p, int t)
 {
-    if (p.decode_mode) {
-        const int pos = p.positions[t];
-        return (pos >= 0 && pos < p.max_seq && pos < p.pages * kPageSize) ? pos / kPageSize + 1 : 0;
-    }
-    const int len = p.tok_len[t];
-    return len > 0 ? (len + kPageSize - 1) / kPageSize : 0;
+    return p.decode_mode ? p.positions[t] : p.tok_len[t];
 }
+
+__device__ __forceinline__ int npg_from(const AttnParams& p, int v)
+{
+    if (p.decode_mode) return (v >= 0 && v < p.max_seq && v < p.pages * kPageSize) ? v / kPageSize + 1 : 0;
+    return v > 0 ? (v + kPageSize - 1) / kPageSize : 0;
+}
+
+__device__ __forceinline__ int npg_of(const AttnParams& p, int t) { return npg_from(p, tok_value(p, t)); }
 
 __device__ __forceinline__ void token_info(const AttnParams& p, int t, int& row, int& len)
 {
@@ -575,7 +582,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     int* sScan = reinterpret_cast<int*>(sbase + L::kScan);
     int* sT0 = reinterpret_cast<int*>(sbase + L::kSum);
     int* sP0 = sT0 + kAttnThreads;
-    int* sN = reinterpret_cast<int*>(sbase + L::kN);
+    int* sN = reinterpret_cast<int*>(sbase + L::kTokN);
+    int* sLen = reinterpret_cast<int*>(sbase + L::kTokLen);
+    int* sRow = reinterpret_cast<int*>(sbase + L::kTokRow);
     uint2* sW = reinterpret_cast<uint2*>(sbase + L::kW);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -610,25 +619,37 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     // which keeps the stream's completion order.
     if (!p.late_wait) pdl_wait();
 
-    // the norm weights, read once here (under the kernel's own streaming a
-    // global load can wait microseconds)
-    if (!p.prepared) {
-        if (tid < 32) sW[tid] = reinterpret_cast<const uint2*>(p.qw)[tid];
-        else if (tid < 64) sW[tid] = reinterpret_cast<const uint2*>(p.kw)[tid - 32];
-    }
-
-    // ---- pages per token and their exclusive prefix over tokens (every CTA computes it)
+    // ---- pages per token and their exclusive prefix over tokens (every CTA computes it).
+    // The norm weights (read once here: under the kernel's own streaming a global load
+    // can wait microseconds) and the first kBatch tokens' positions of each thread are
+    // loaded together, one round trip.
+    constexpr int kBatch = 4;
+    const bool wload = !p.prepared && tid < 64;
+    uint2 wv = make_uint2(0u, 0u);
+    if (wload) wv = reinterpret_cast<const uint2*>(tid < 32 ? p.qw : p.kw)[tid & 31];
     const int nt = p.ntok;
     const int per = (nt + kAttnThreads - 1) / kAttnThreads;
     const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
+    int tv[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) tv[k] = t0 + k < t1 ? tok_value(p, t0 + k) : 0;
+    const int trow = (per == 1 && t0 < t1) ? (p.decode_mode ? t0 : p.tok_row[t0]) : 0;
     int local = 0, lmax = 0, lnz = 0;  // pages, the longest unit, tokens with pages
-    for (int t = t0; t < t1; ++t) {
-        const int n = npg_of(p, t);
+    auto count = [&](int n) {
         local += n;
         lmax = max(lmax, n);
         lnz += n > 0;
+    };
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+        if (t0 + k < t1) count(npg_from(p, tv[k]));
+    for (int t = t0 + kBatch; t < t1; ++t) count(npg_of(p, t));
+    if (wload) sW[tid] = wv;
+    if (per == 1) {  // every token has its own thread: what the whole-unit split reads
+        sN[tid] = local;
+        sLen[tid] = p.decode_mode ? tv[0] + 1 : tv[0];
+        sRow[tid] = trow;
     }
-    if (per == 1) sN[tid] = local;  // (read only when every token has its own thread)
     int incl = local, wmax = lmax, wnz = lnz;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -674,16 +695,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             // thread whose run of tokens holds it, so that the producer starts without a search
             const int64_t x0 = (int64_t)c * sp.S / sp.Ce;
             int run = excl;
-            if (x0 >= (int64_t)G * run && x0 < (int64_t)G * (run + local))
-                for (int t = t0; t < t1; ++t) {
-                    const int n = npg_of(p, t);
-                    if (n > 0 && x0 < (int64_t)G * (run + n)) {
+            if (x0 >= (int64_t)G * run && x0 < (int64_t)G * (run + local)) {
+                bool found = false;
+                auto look = [&](int t, int n) {
+                    if (!found && n > 0 && x0 < (int64_t)G * (run + n)) {
                         sScan[24] = t;
                         sScan[25] = run;
-                        break;
+                        found = true;
                     }
                     run += n;
-                }
+                };
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k)
+                    if (t0 + k < t1) look(t0 + k, npg_from(p, tv[k]));
+                for (int t = t0 + kBatch; t < t1 && !found; ++t) look(t, npg_of(p, t));
+            }
         }
     }
     if (c == 0) {
@@ -739,12 +765,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             int64_t St = (int64_t)G * pre;  // global index of (t, kv head 0, page 0)
             int64_t x = xb;
             while (x < xe && ok) {
-                const int n = npg_of(p, t);
+                const int n = sp.whole ? sN[t] : npg_of(p, t);
                 const int64_t off = x - St;
                 const int g = (int)(off / n), j = (int)(off % n);
                 const int seg = (int)min((int64_t)(n - j), xe - x);
                 int row, len;
-                token_info(p, t, row, len);
+                if (sp.whole) {
+                    row = sRow[t];
+                    len = sLen[t];
+                } else {
+                    token_info(p, t, row, len);
+                }
                 const int pos = len - 1;
                 // lane 0: the table entry of page jj; lanes 1 and 2: the same column of the rows
                 // before and after, so that a prefix page shared with a neighbouring row is known
