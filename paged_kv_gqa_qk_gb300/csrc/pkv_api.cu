@@ -44,7 +44,7 @@ Plan make_plan(const pkv_pool* pool, int tokens, int pages, int prompt_tokens)
     pl.off_row = off;
     off = align_up(off + sizeof(int32_t) * tokens, 256);
     pl.off_prefix = off;
-    off = align_up(off + sizeof(int32_t) * (tokens + 1), 256);
+    off = align_up(off + sizeof(int32_t) * (tokens + 2), 256);
     pl.off_unit_ok = off;
     off = align_up(off + sizeof(int32_t) * units, 256);
     pl.off_po = off;
@@ -75,7 +75,7 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
     if (!decode && a.steps == 0) {  // prompts only: prep -> prompt-token attention (the timed kernel)
         if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
         if (timed && cudaEventRecord(pool->ev_start[slot], s) != cudaSuccess) return PKV_ECUDA;
-        if (launch_prefill(pool, a, plan, pool->num_sms, s) != cudaSuccess) return PKV_ECUDA;
+        if (launch_prefill(pool, a, plan, pool->num_sms, false, s) != cudaSuccess) return PKV_ECUDA;
         if (timed && cudaEventRecord(pool->ev_stop[slot], s) != cudaSuccess) return PKV_ECUDA;
         return PKV_OK;
     }
@@ -84,7 +84,9 @@ int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s)
     ps.claim = pool->claims + (pool->call_seq++ % kClaimSlots);
     if (!decode) {
         if (launch_prep(pool, a, plan, s) != cudaSuccess) return PKV_ECUDA;
-        if (launch_prefill(pool, a, plan, pool->num_sms, s) != cudaSuccess) return PKV_ECUDA;
+        // beside the step rows' attention (programmatic launch), the prompt attention keeps
+        // part of the SMs and leaves the rest to it (prompt_sms); timed calls run them in turn
+        if (launch_prefill(pool, a, plan, pool->num_sms, !timed, s) != cudaSuccess) return PKV_ECUDA;
         // the step rows are tokens P..P+rows-1
         const size_t qrow = (size_t)pool->cfg.heads * pool->cfg.head_dim * 2;
         as.q = static_cast<const char*>(a.q) + (size_t)a.P * qrow;

@@ -114,6 +114,36 @@ __device__ __forceinline__ int page_of(const int32_t* table, int pages, int row,
     return table ? table[(int64_t)row * pages + j] : row * pages + j;
 }
 
+// A step's SMs, split between the prompt attention and the step rows' attention.
+// The prompt attention keeps prompt_sms(...) SMs and the rows' attention starts
+// on the others at once (it is launched when every prompt-attention CTA has
+// started, so its CTAs land on the SMs the ones beyond the kept count leave);
+// both kernels derive the split from the same token lengths, so they agree.
+// Costs are in 1/25 µs of one SM: a prompt unit (64-token tile, kv head) 6.4 µs
+// plus 1.12 µs a page of its longest token (the prompt attention's measured
+// rate, start and tail included), a step row's page of one kv head 0.52 µs (32
+// KiB at ~60 GB/s, what one SM streams when the rows have part of the chip).
+constexpr int64_t kSplitPromptUnit = 160, kSplitPromptPage = 28, kSplitRowPage = 13;
+constexpr int kSplitMinRowSms = 8;  // leaving the rows fewer SMs than this: no split
+
+__host__ __device__ inline int prompt_sms(int64_t prompt_cost, int64_t row_cost, int prompt_units, int sms)
+{
+    if (prompt_cost <= 0 || row_cost <= 0) return sms;
+    int n = (int)((prompt_cost * sms + (prompt_cost + row_cost) / 2) / (prompt_cost + row_cost));
+    const int few = prompt_units < sms / 4 ? prompt_units : sms / 4;  // each of a few units its own SM
+    n = n > few ? n : few;
+    if (n < 1) n = 1;
+    return n > sms - kSplitMinRowSms ? sms : n;
+}
+
+// Cost of one prompt tile (whose tokens' attended lengths have maximum max_len)
+// in the units above, over its kv heads; 0 for a tile with no token.
+__host__ __device__ inline int64_t prompt_tile_cost(int max_len, int kv_heads)
+{
+    return max_len > 0 ? (int64_t)kv_heads * (kSplitPromptUnit + kSplitPromptPage * ((max_len + kPageSize - 1) / kPageSize))
+                       : 0;
+}
+
 // 2-D tiled tensor map of a row-major bf16 matrix (128-byte swizzle, zero fill
 // past the edges); false if the driver refuses it.
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
@@ -163,7 +193,10 @@ cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& 
                            cudaStream_t s);
 // step mode: prompt-token attention on tcgen05 tensor cores (pkv_prefill.cu), a
 // persistent grid of `ctas` CTAs (one per SM; capped at its work units)
-cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, cudaStream_t s);
+// split: the step rows' attention is launched beside it (programmatic launch); the
+// kernel then keeps only prompt_sms(...) of its CTAs (see prompt_sms).
+cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, bool split,
+                           cudaStream_t s);
 
 // Enqueue one decode (a.P == 0) or step call on workspace a.ws; host checks done.
 int enqueue(pkv_pool* pool, const StepArgs& a, const Plan& plan, cudaStream_t s);

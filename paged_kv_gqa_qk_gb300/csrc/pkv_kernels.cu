@@ -347,7 +347,7 @@ struct AttnParams {
     float* part_o;            // [U + C (1 + kDynChunksPerCta)][4][128]
     float* part_lse;          // [U + C (1 + kDynChunksPerCta)][4]
     uint32_t* claim;          // chunk counter, zero at launch
-    int32_t* prefix;          // [ntok + 1], written by CTA 0 for combine_kernel
+    int32_t* prefix;          // [ntok + 2], written by CTA 0 for combine_kernel: prefix, total, resident CTAs
     int32_t* unit_ok;         // [U], by the CTA holding each unit's first page: 0 invalid, 1 cut, 2 written out
     uint32_t* err;
     int ntok, pages, num_pages, max_seq, heads, kv_heads, decode_mode, rot;
@@ -357,6 +357,8 @@ struct AttnParams {
     int64_t num_slots;
     float eps;
     uint64_t wait_ns;         // limit of the ring and group waits (the final drain always allows kWaitLimitNs)
+    int prompt_P;             // step mode: the call's prompt tokens (their lengths precede tok_len), else 0
+    int sms, ctas_per_sm;     // the device's SMs, and this kernel's resident CTAs per SM
 };
 
 constexpr int kConsumerWarps = 4;
@@ -388,7 +390,8 @@ struct AttnSmem {
     static constexpr int kTokN = kSum + 2 * kAttnThreads * 4;
     static constexpr int kTokLen = kTokN + kAttnThreads * 4;
     static constexpr int kTokRow = kTokLen + kAttnThreads * 4;
-    static constexpr int kW = kTokRow + kAttnThreads * 4;     // bf16 q_norm_w [128], k_norm_w [128]
+    static constexpr int kSplit = kTokRow + kAttnThreads * 4;  // per warp: int64 prompt cost [8], int units [8]
+    static constexpr int kW = kSplit + 8 * 8 + 8 * 4;         // bf16 q_norm_w [128], k_norm_w [128]
     static constexpr int kBars = kW + 512;                    // u64 full[S], empty[S], group
     static constexpr int kFlag = kBars + 8 * (2 * kStages + 1);  // int abort, items issued, stop item sent
     static constexpr int kBytes = kFlag + 16;
@@ -663,6 +666,35 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         sScan[8 + warp] = wmax;
         sScan[16 + warp] = wnz;
     }
+    if (p.prompt_P > 0) {
+        // a step: the prompt attention's cost (prompt_tile_cost over the prompt tiles), for
+        // the split of the SMs; warp w takes tiles w, w + 5, ..., kTB of them a round trip
+        const int32_t* plen = p.tok_len - p.prompt_P;  // the prompt tokens' attended lengths
+        const int ptiles = (p.prompt_P + 63) / 64;
+        constexpr int kTB = 8, kWarps = kAttnThreads / 32;
+        int64_t pc = 0;
+        int pu = 0;
+        for (int tb = warp; tb < ptiles; tb += kTB * kWarps) {
+            int m[kTB][2];
+#pragma unroll
+            for (int b = 0; b < kTB; ++b)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int tok = (tb + b * kWarps) * 64 + lane + 32 * i;
+                    m[b][i] = (tb + b * kWarps < ptiles && tok < p.prompt_P) ? plen[tok] : 0;
+                }
+#pragma unroll
+            for (int b = 0; b < kTB; ++b) {
+                const int mx = (int)__reduce_max_sync(kFull, (uint32_t)max(max(m[b][0], m[b][1]), 0));
+                pc += prompt_tile_cost(mx, G);
+                pu += mx > 0 ? G : 0;
+            }
+        }
+        if (lane == 0) {
+            reinterpret_cast<int64_t*>(sbase + L::kSplit)[warp] = pc;
+            reinterpret_cast<int*>(sbase + L::kSplit + 64)[warp] = pu;
+        }
+    }
     __syncthreads();
     int total = 0, warp_base = 0, nmax = 0, nz = 0;
 #pragma unroll
@@ -675,7 +707,23 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
     const int excl = warp_base + incl - local;
     const int64_t T = (int64_t)G * total;
-    const Split sp = whole_units(nt, nmax, T, C) ? whole_split(G * nz, C) : split_of(T, C);
+    // Ra: the CTAs resident from the start, which hold the static slices (or first units).
+    // In a step the prompt attention keeps some SMs (prompt_sms), and this grid starts on
+    // the others; its CTAs beyond Ra start when the prompt attention ends, and claim chunks.
+    int Ra = C;
+    if (p.prompt_P > 0) {
+        int64_t pc = 0;
+        int pu = 0;
+#pragma unroll
+        for (int w = 0; w < kAttnThreads / 32; ++w) {
+            pc += reinterpret_cast<const int64_t*>(sbase + L::kSplit)[w];
+            pu += reinterpret_cast<const int*>(sbase + L::kSplit + 64)[w];
+        }
+        const int pgrid = min(p.sms, ((p.prompt_P + 63) / 64) * G);  // the prompt attention's grid
+        const int kept = min(prompt_sms(pc, kSplitRowPage * T, pu, p.sms), pgrid);  // the SMs it holds
+        if (kept < p.sms) Ra = max(1, min(C, p.ctas_per_sm * (p.sms - kept)));
+    }
+    const Split sp = whole_units(nt, nmax, T, Ra) ? whole_split(G * nz, Ra) : split_of(T, Ra);
     if (sp.whole) {
         // tokens longest first (ties by index): sT0[rank] = the token, sP0[rank] = its prefix
         if (tid < nt && local > 0) {
@@ -718,10 +766,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             p.prefix[t] = run;
             run += npg_of(p, t);
         }
-        if (tid == kAttnThreads - 1) p.prefix[nt] = total;
+        if (tid == kAttnThreads - 1) {
+            p.prefix[nt] = total;
+            p.prefix[nt + 1] = Ra;  // the combine derives the same intervals
+        }
     }
     __syncthreads();
-    if (c >= sp.Ce) {
+    if (c >= sp.Ce && !sp.ND) {  // no static slice and nothing to claim
         if (p.late_wait) pdl_wait();
         return;
     }
@@ -738,8 +789,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         // the range before it has kClaimAhead pages left to issue: late enough that
         // the CTAs finishing first take the chunks, early enough that the
         // counter's answer is there when the range ends.
+        // (A CTA beyond the Ce static slices -- one started late, in a step -- has no
+        // first range and claims at once.)
+        bool stat = c < sp.Ce;  // the range is this CTA's static slice (or first unit)
+        bool have = stat;       // there is a range to issue
         int64_t xb = 0, xe = 0;
-        if (!sp.whole) {
+        if (!sp.whole && stat) {
             xb = (int64_t)c * sp.S / sp.Ce;
             xe = (int64_t)(c + 1) * sp.S / sp.Ce;
         }
@@ -748,15 +803,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         uint32_t claim = 0;
         bool want = sp.ND > 0;  // the next chunk is still to be claimed
         for (;;) {
-            int t, pre;
-            if (sp.whole) {  // one unit, never cut: no partials
+            int t = 0, pre = 0;
+            if (!have) {
+                xb = xe = 0;
+            } else if (sp.whole) {  // one unit, never cut: no partials
                 t = sT0[unit / G];
                 pre = sP0[unit / G];
                 const int n = sN[t];
                 xb = (int64_t)G * pre + (int64_t)(unit % G) * n;
                 xe = xb + n;
                 iv = 0;
-            } else if (iv == c) {  // the static slice: its first token was found in the prologue
+            } else if (stat) {  // the static slice: its first token was found in the prologue
                 t = sScan[24];
                 pre = sScan[25];
             } else {
@@ -868,6 +925,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             want = true;
             const uint32_t k = __shfl_sync(kFull, claim, 0);
             if (k >= (uint32_t)sp.ND) break;
+            stat = false;
+            have = true;
             unit = sp.Ce + (int)k;
             xb = sp.S + (int64_t)k * sp.Q;
             xe = xb + sp.Q;
@@ -1240,6 +1299,10 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
     p.qhat = a.q_hat;
     p.prepared = a.q_hat ? 1 : 0;
     p.late_wait = (!decode_mode && pdl) ? 1 : 0;
+    // a step whose prompt attention runs beside this kernel (programmatic launch) splits the SMs
+    p.prompt_P = p.late_wait ? a.P : 0;
+    p.sms = pool->num_sms;
+    p.ctas_per_sm = pool->ctas_per_sm;
     p.rot = pool->cfg.rotary_dim > 0 ? pool->cfg.rotary_dim : kHeadDim;
     p.num_slots = pool->num_slots;
     p.eps = static_cast<float>(pool->cfg.eps);
@@ -1262,7 +1325,7 @@ cudaError_t launch_attn(const pkv_pool* pool, const StepArgs& a, const Plan& pla
 // combine_kernel
 // =====================================================================================
 struct CombineParams {
-    const int32_t* prefix;    // [ntok + 1]
+    const int32_t* prefix;    // [ntok + 2]: page prefix, total, the attention's resident CTAs
     const int32_t* unit_ok;   // [U]
     const int32_t* positions; // decode mode: [ntok]
     const float* part_o;
@@ -1270,7 +1333,7 @@ struct CombineParams {
     __nv_bfloat16* out;
     uint32_t* err;
     uint32_t* claim;          // the attention's chunk counter: zeroed here for the call that next uses it
-    int ntok, heads, kv_heads, ctas, decode_mode;
+    int ntok, heads, kv_heads, decode_mode;
 };
 
 // One CTA per (token, kv head) unit; warp w = query head 4g+w, lane owns dims 4*lane..4*lane+3.
@@ -1290,7 +1353,7 @@ __global__ void __launch_bounds__(128 * kWph) combine_kernel(CombineParams p)
     if (u == 0 && threadIdx.x == 0) *p.claim = 0;  // the attention grid has finished claiming
     __nv_bfloat16* dst = p.out + ((int64_t)t * p.heads + h) * kHeadDim + 4 * lane;
     // every index this CTA needs, loaded together (one round trip)
-    const int pre = p.prefix[t], pre1 = p.prefix[t + 1], total = p.prefix[p.ntok];
+    const int pre = p.prefix[t], pre1 = p.prefix[t + 1], total = p.prefix[p.ntok], ra = p.prefix[p.ntok + 1];
     const int uok = p.unit_ok[u];
     const int n = pre1 - pre;
     if (n == 0) {  // skipped token
@@ -1307,7 +1370,7 @@ __global__ void __launch_bounds__(128 * kWph) combine_kernel(CombineParams p)
     }
     if (uok == 2) return;  // one range held the whole unit, and its CTA wrote it out
     const int64_t T = (int64_t)G * total;
-    const Split sp = split_of(T, p.ctas);  // the attention kernel's intervals
+    const Split sp = split_of(T, ra);  // the attention kernel's intervals (ra: its static slices' CTAs)
     const int64_t S = (int64_t)G * pre + (int64_t)g * n;
     const int64_t rf = interval_of(S, sp), rl = interval_of(S + n - 1, sp);
     if (rf == rl) return;  // one interval held the whole unit, and its CTA wrote it out
@@ -1396,7 +1459,6 @@ cudaError_t launch_combine(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.ntok = plan.tokens;
     p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
-    p.ctas = plan.ctas;
     p.decode_mode = decode_mode ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((int64_t)plan.tokens * pool->cfg.kv_heads));

@@ -78,7 +78,8 @@ struct PfSmem {
     static constexpr int kSort = kRing + kPfStages * kPfStageBytes;  // uint32 [kMaxSortTiles]
     static constexpr int kTok = kSort + 4 * kMaxSortTiles;          // int pos[64], row[64]
     static constexpr int kRuns = kTok + 2 * kTileTok * 4;           // int row[64], npages[64], count, unit
-    static constexpr int kBars = kRuns + (2 * kTileTok + 4) * 4;
+    static constexpr int kSplit = kRuns + (2 * kTileTok + 4) * 4;   // u64 prompt cost, prompt units, row pages
+    static constexpr int kBars = kSplit + 32;
     // full[S], empty[S], s_ready[2], p_ready[2], o_done[2], epi[2], drain, q_full
     static constexpr int kNumBars = 2 * kPfStages + 4 * kGroups + 2;
     static constexpr int kTmemSlot = kBars + 8 * kNumBars;
@@ -97,6 +98,9 @@ struct PfParams {
     int32_t* sched;           // unit counter, zero at launch
     uint32_t* err;
     int P, pages, heads, kv_heads, ntiles;
+    int split;                // 1: the step rows' attention runs beside this grid (see prompt_sms); the
+                              // kernel instantiated with kSplit = true runs it
+    int steps, sms;           // the step rows (tokens P..P+steps-1 of the token table), the device's SMs
 };
 
 
@@ -598,6 +602,8 @@ __device__ __forceinline__ void idle_role(const PfCtx& c)
     }
 }
 
+// kSplit: a step whose rows' attention runs beside this grid (PfParams::split).
+template <bool kSplit>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, PfParams p)
@@ -654,7 +660,58 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     pdl_launch_dependents();
     // the producer's first unit is claimed now; the answer is needed after the sort
     int first_claim = 0;
-    if (warp == kProducer && lane == 0) first_claim = atomicAdd(p.sched, 1);
+    if (!kSplit && warp == kProducer && lane == 0) first_claim = atomicAdd(p.sched, 1);
+    if (kSplit) {
+        // The step rows' attention runs beside this grid: only the first prompt_sms(...)
+        // CTAs go on, the others end here and leave their SMs to it (it derives the same
+        // count from the same token lengths).  Warp w sums prompt_tile_cost over tiles
+        // w, w + 12, ... (kTB tiles a round trip); every thread sums its rows' pages.
+        unsigned long long* sSplit = reinterpret_cast<unsigned long long*>(c.sbase + PfSmem::kSplit);
+        if (tid < 3) sSplit[tid] = 0ull;
+        __syncthreads();
+        constexpr int kWarps = kPfThreads / 32, kTB = 4;
+        int64_t pc = 0, rp = 0;
+        int pu = 0;
+        for (int tb = warp; tb < p.ntiles; tb += kTB * kWarps) {
+            int m[kTB][2];
+#pragma unroll
+            for (int b = 0; b < kTB; ++b)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int tok = (tb + b * kWarps) * kTileTok + lane + 32 * i;
+                    m[b][i] = (tb + b * kWarps < p.ntiles && tok < p.P) ? p.tok_len[tok] : 0;
+                }
+#pragma unroll
+            for (int b = 0; b < kTB; ++b) {
+                const int mx = (int)__reduce_max_sync(kAll, (uint32_t)max(max(m[b][0], m[b][1]), 0));
+                pc += prompt_tile_cost(mx, p.kv_heads);
+                pu += mx > 0 ? p.kv_heads : 0;
+            }
+        }
+        for (int r = tid; r < p.steps; r += kPfThreads) {
+            const int len = p.tok_len[p.P + r];
+            rp += len > 0 ? (len + kPageSize - 1) / kPageSize : 0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rp += __shfl_xor_sync(kAll, rp, o);
+        if (lane == 0) {
+            if (pc) atomicAdd(&sSplit[0], (unsigned long long)pc);
+            if (pu) atomicAdd(&sSplit[1], (unsigned long long)pu);
+            if (rp) atomicAdd(&sSplit[2], (unsigned long long)rp);
+        }
+        tc_fence_before();
+        __syncthreads();
+        const int keep = prompt_sms((int64_t)sSplit[0], kSplitRowPage * p.kv_heads * (int64_t)sSplit[2],
+                                    (int)sSplit[1], p.sms);
+        if ((int)blockIdx.x >= keep) {  // this CTA ends here, its tensor memory freed first
+            if (warp == kIssuer) {
+                tc_fence_after();
+                tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(c.sbase + PfSmem::kTmemSlot), kTmemCols);
+            }
+            return;
+        }
+        if (warp == kProducer && lane == 0) first_claim = atomicAdd(p.sched, 1);
+    }
 
     // ---- work items: the runs of every tile (a tile with none is one empty item,
     // so that its skipped tokens still get their zero output), in decreasing order
@@ -765,13 +822,18 @@ cudaError_t configure_prefill()
     // The kernel moves registers between its warpgroups assuming it is launched
     // with exactly kRegsLaunch per thread; refuse to run it with any other count.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != (int)kRegsLaunch) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem::kAlloc);
+    for (auto k : {prefill_kernel<false>, prefill_kernel<true>}) {
+        cudaError_t e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != (int)kRegsLaunch) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem::kAlloc);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
-cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, cudaStream_t s)
+cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& plan, int ctas, bool split,
+                           cudaStream_t s)
 {
     PfParams p;
     p.tok_len = reinterpret_cast<const int32_t*>(a.ws + plan.off_len);
@@ -785,6 +847,9 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     p.heads = pool->cfg.heads;
     p.kv_heads = pool->cfg.kv_heads;
     p.ntiles = (a.P + kTileTok - 1) / kTileTok;
+    p.split = split && a.steps > 0 ? 1 : 0;
+    p.steps = a.steps;
+    p.sms = pool->num_sms;
     // the prompt tokens' queries prep_kernel prepared in the workspace
     CUtensorMap tmQ;
     if (!make_tmap_heads(&tmQ, a.ws + plan.off_qhat, p.heads, a.P)) return cudaErrorInvalidValue;
@@ -800,7 +865,8 @@ cudaError_t launch_prefill(const pkv_pool* pool, const StepArgs& a, const Plan& 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel, pool->tmap_k, pool->tmap_v, tmQ, p);
+    return p.split ? cudaLaunchKernelEx(&cfg, prefill_kernel<true>, pool->tmap_k, pool->tmap_v, tmQ, p)
+                   : cudaLaunchKernelEx(&cfg, prefill_kernel<false>, pool->tmap_k, pool->tmap_v, tmQ, p);
 }
 
 }  // namespace pkv

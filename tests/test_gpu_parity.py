@@ -97,6 +97,50 @@ def test_step_small_with_explicit_slots():
     compare(wl, run_gpu(wl, ctas=13), ref, label="step ctas=13")
 
 
+def _step_sm_split(wl):
+    """The kernels' split of a step's SMs (prompt_sms in csrc/pkv_internal.h):
+    (SMs the prompt attention holds, the rows' attention CTAs resident from the
+    start).  Costs in 1/25 us of one SM."""
+    S, G = wl.cfg["page_size"], wl.cfg["kv_heads"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    lens = (wl.positions + 1).tolist()
+    pc, pu = 0, 0
+    for t0 in range(0, len(lens), 64):
+        m = max(lens[t0:t0 + 64])
+        if m > 0:
+            pc += G * (160 + 28 * ((m + S - 1) // S))
+            pu += G
+    rc = 13 * G * sum(p // S + 1 for p in wl.step_positions.tolist() if p >= 0)
+    n = sms
+    if pc > 0 and rc > 0:
+        n = (pc * sms + (pc + rc) // 2) // (pc + rc)
+        n = max(n, min(pu, sms // 4), 1)
+        n = sms if n > sms - 8 else n
+    pgrid = min(sms, (len(lens) + 63) // 64 * G)
+    kept = min(n, pgrid)
+    return kept, (2 * (sms - kept) if kept < sms else 2 * sms)
+
+
+def test_step_prompts_beside_the_rows():
+    """A step whose prompt attention keeps part of the SMs (prompt_sms) while
+    the rows' attention starts on the rest: 4 prompt chunks continuing long
+    rows, 64 rows of 2K-4K positions; then short rows (whole units) beside one
+    small chunk, where the rows' attention CTAs that start late only claim."""
+    wl = W.make_step("prompts beside rows", prompt_lengths=[128, 128, 128, 128], prompt_starts=[600, 1500, 0, 3000],
+                     decode_lengths=W._uniform_int(torch.Generator().manual_seed(41), 2048, 4096, 64).tolist(),
+                     seed=41, table_pages=64)
+    kept, ra = _step_sm_split(wl)
+    assert kept < min(torch.cuda.get_device_properties(0).multi_processor_count, 8 * 8), kept
+    ref = run_oracle(wl)
+    compare(wl, run_gpu(wl), ref, label="prompts beside rows")
+    short = W.make_step("chunk beside short rows", prompt_lengths=[64], prompt_starts=[100],
+                        decode_lengths=W._uniform_int(torch.Generator().manual_seed(42), 1, 512, 100).tolist(),
+                        seed=42, table_pages=8)
+    kept, ra = _step_sm_split(short)
+    assert ra < 2 * torch.cuda.get_device_properties(0).multi_processor_count, ra
+    compare(short, run_gpu(short), run_oracle(short), label="chunk beside short rows")
+
+
 @pytest.mark.parametrize("ctas", [0, 7])
 def test_new_key_dominates(ctas):
     """Each row's new key equals its first query head's (same raw vector, same
