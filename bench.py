@@ -106,6 +106,9 @@ def make_workload(name: str, rank: int = 0):
         wl = W.prefill_mix(seed=rank_seed(1006, rank))
     elif name == "rows":
         wl = W.rows_mix(seed=rank_seed(1007, rank))
+    elif name == "short256":
+        wl = W.make_decode("decode 256 short rows x U[1,1024]", (256, 1, 1024), seed=rank_seed(1008, rank),
+                           table_pages=16)
     elif name.startswith("sweep"):
         r, l = name[5:].split("x")
         wl = W.sweep(int(r), int(l), seed=rank_seed(2000 + int(r) + int(l), rank))
