@@ -97,3 +97,26 @@ def compare(wl, gpu, ref, sel=None, label=""):
     assert max_abs <= MAX_ABS, f"{label}: max-abs {max_abs:.3e} > {MAX_ABS}"
     assert rel <= REL_L2, f"{label}: rel-L2 {rel:.3e} > {REL_L2}"
     return max_abs, rel
+
+
+def step_sm_split(prompt_lens, step_positions, kv_heads: int, sms: int, page_size: int = 64):
+    """The kernels' split of a step's SMs (prompt_sms and prompt_tile_cost in
+    csrc/pkv_internal.h): (SMs the prompt attention holds, the rows' attention
+    CTAs resident from the start at two a SM).  prompt_lens: attended lengths
+    of the prompt tokens (0 skipped); costs in 1/25 us of one SM."""
+    G, S = kv_heads, page_size
+    pc, pu = 0, 0
+    for t0 in range(0, len(prompt_lens), 64):
+        m = max(prompt_lens[t0:t0 + 64])
+        if m > 0:
+            pc += G * (160 + 28 * ((m + S - 1) // S))
+            pu += G
+    rc = 13 * G * sum(p // S + 1 for p in step_positions if p >= 0)
+    n = sms
+    if pc > 0 and rc > 0:
+        n = (pc * sms + (pc + rc) // 2) // (pc + rc)
+        n = max(n, min(pu, sms // 4), 1)
+        n = sms if n > sms - 8 else n
+    pgrid = min(sms, (len(prompt_lens) + 63) // 64 * G)
+    kept = min(n, pgrid)
+    return kept, (2 * (sms - kept) if kept < sms else 2 * sms)

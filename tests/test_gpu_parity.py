@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_kv_gqa_qk_gb300 as pkv
 import workloads as W
-from _harness import compare, run_gpu, run_oracle
+from _harness import compare, run_gpu, run_oracle, step_sm_split
 
 pytestmark = pytest.mark.gpu
 
@@ -98,27 +98,8 @@ def test_step_small_with_explicit_slots():
 
 
 def _step_sm_split(wl):
-    """The kernels' split of a step's SMs (prompt_sms in csrc/pkv_internal.h):
-    (SMs the prompt attention holds, the rows' attention CTAs resident from the
-    start).  Costs in 1/25 us of one SM."""
-    S, G = wl.cfg["page_size"], wl.cfg["kv_heads"]
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    lens = (wl.positions + 1).tolist()
-    pc, pu = 0, 0
-    for t0 in range(0, len(lens), 64):
-        m = max(lens[t0:t0 + 64])
-        if m > 0:
-            pc += G * (160 + 28 * ((m + S - 1) // S))
-            pu += G
-    rc = 13 * G * sum(p // S + 1 for p in wl.step_positions.tolist() if p >= 0)
-    n = sms
-    if pc > 0 and rc > 0:
-        n = (pc * sms + (pc + rc) // 2) // (pc + rc)
-        n = max(n, min(pu, sms // 4), 1)
-        n = sms if n > sms - 8 else n
-    pgrid = min(sms, (len(lens) + 63) // 64 * G)
-    kept = min(n, pgrid)
-    return kept, (2 * (sms - kept) if kept < sms else 2 * sms)
+    return step_sm_split((wl.positions + 1).tolist(), wl.step_positions.tolist(), wl.cfg["kv_heads"],
+                         torch.cuda.get_device_properties(0).multi_processor_count, wl.cfg["page_size"])
 
 
 def test_step_prompts_beside_the_rows():
