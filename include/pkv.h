@@ -416,7 +416,11 @@ PKV_API int pkv_set_wait_limit(pkv_pool* pool, int64_t ns);
  * enable: 0 off, 1 every launch named above, 2 the attention launches only
  * (not pkv_linear / pkv_qkv_proj / pkv_qkv_proj_append); PKV_EINVAL otherwise.  Host
  * threads sharing a pool take distinct event slots; pkv_timer_enable and
- * pkv_timer_read should not race with calls in flight on other threads. */
+ * pkv_timer_read should not race with calls in flight on other threads.
+ * A timed pkv_step runs its prompt attention and its step rows' attention one
+ * after the other (the events between them), where an untimed one runs them
+ * side by side on a split of the SMs: the timer measures the rows' attention
+ * alone, not the step. */
 PKV_API int pkv_timer_enable(pkv_pool* pool, int enable);
 PKV_API int pkv_timer_read(pkv_pool* pool, double* total_ms, int64_t* launches);
 
