@@ -122,6 +122,20 @@ def test_step_prompts_beside_the_rows():
     compare(short, run_gpu(short), run_oracle(short), label="chunk beside short rows")
 
 
+def test_step_many_prompt_tiles_beside_the_rows():
+    """More prompt tiles (54 of 64 tokens) than either kernel's cost pass covers
+    in one round trip, so both derive the split over several rounds; the
+    prompt attention still keeps part of the SMs."""
+    g = torch.Generator().manual_seed(43)
+    wl = W.make_step("many prompt tiles", prompt_lengths=[550] * 6,
+                     prompt_starts=W._uniform_int(g, 0, 1500, 6).tolist(),
+                     decode_lengths=W._uniform_int(g, 1024, 4096, 48).tolist(), seed=43, table_pages=64)
+    assert wl.P > 3072
+    kept, ra = _step_sm_split(wl)
+    assert kept < torch.cuda.get_device_properties(0).multi_processor_count, kept
+    compare(wl, run_gpu(wl), run_oracle(wl), label="many prompt tiles")
+
+
 @pytest.mark.parametrize("ctas", [0, 7])
 def test_new_key_dominates(ctas):
     """Each row's new key equals its first query head's (same raw vector, same
